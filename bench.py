@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark: effective KV-read bandwidth of paged fp8 verify attention on GB300.
+
+One step = one call of the whole op (split-KV main kernel + segment reduce)
+over one batch.  Default workload: 16 sequences x 35000 keys, q_len 4, 16 query
+heads on 1 KV head, head_dim 256, page 16 fp8 e4m3, k/v descales 0.5 / 2.0,
+num_segments 16, block tables randomly permuted over a page pool that holds 8
+rotating KV replicas (2.29 GB, far above the 129 MB L2), so every timed call
+reads its K/V from HBM.
+
+    effective TB/s = sum_b C_b * H_kv * 256 * 2 bytes / time per call
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU runs are independent replicas (the op shards into independent
+(sequence, KV head) units with no exchange): value = all ranks' bytes / the
+slowest rank's time.  `--impl reference` times the CPU oracle on the host cores
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective KV-read TB/s and us/call (16x35k, GQA16) vs GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="verify_16x35k_gqa16")
+    ap.add_argument("--segments", type=int, default=16)
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--warm-seconds", type=float, default=1.0,
+                    help="keep warming up at least this long (steady clocks and power)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ceiling-gib", type=float, default=4.0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm, and the cpu_baseline of our arm)
+
+def _oracle_worker(job):
+    """Build one sequence of the workload on the host and time the oracle on it."""
+    import torch
+    import oracle
+    from paged_fp8_speculative_gb300 import synth
+    ctx, ql, hq, hkv, kd, vd, seed = job
+    b = synth.make_batch([ctx], [ql], hq, hkv, seed=seed, k_descale=kd, v_descale=vd)
+    args = (b.q.view(torch.int16).numpy(), b.k_cache.numpy(), b.v_cache.numpy(),
+            b.block_tables.numpy(), b.seq_lens.numpy(), b.cu_seqlens_q.numpy(), b.k_descale,
+            b.v_descale, b.softmax_scale, b.num_kv_heads)
+    t0 = time.perf_counter()
+    oracle.verify_attention_rows(*args)
+    return time.perf_counter() - t0, ctx * hkv * 256 * 2
+
+
+def _oracle_jobs(workload: str, n: int):
+    from paged_fp8_speculative_gb300 import synth
+    ctx, ql, hq, hkv, kd, vd = synth.workload_spec(workload)
+    return [(ctx[i % len(ctx)], ql[i % len(ql)], hq, hkv, kd, vd, 123 + i) for i in range(n)]
+
+
+class OraclePool:
+    """A spawn-started process pool (safe next to CUDA in the parent), one BLAS thread each.
+
+    A step runs one sequence per process concurrently; its time is the slowest
+    process's oracle time (input generation excluded)."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs)
+
+    def run(self, jobs):
+        res = self.pool.map(_oracle_worker, jobs, chunksize=1)
+        return max(r[0] for r in res), sum(r[1] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(workload: str) -> dict:
+    procs = min(cpu_cores(), 16)
+    jobs = _oracle_jobs(workload, procs)
+    pool = OraclePool(procs)
+    try:
+        pool.run(jobs[:1])                           # worker start-up and imports
+        dt, kv_bytes = pool.run(jobs)
+    finally:
+        pool.close()
+    return {"value": kv_bytes / dt / 1e12, "unit": "TB/s", "cores": procs, "kind": "oracle",
+            "sample": f"{procs} sequence(s) of the {workload} shape, one per process "
+                      f"(float64 oracle, slowest process {dt:.2f} s)"}
+
+
+def run_reference(a) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    procs = min(cpu_cores(), 16)
+    jobs = _oracle_jobs(a.workload, procs)
+    pool = OraclePool(procs)
+    try:
+        for _ in range(a.warmup):
+            pool.run(jobs)
+        runs = [pool.run(jobs) for _ in range(a.steps)]
+    finally:
+        pool.close()
+    total_t = sum(r[0] for r in runs)
+    value = sum(r[1] for r in runs) / total_t / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TB/s", "impl": "reference",
+            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": 1e3 * total_t / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(a),
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": procs, "kind": "oracle",
+                             "sample": f"each step: {procs} sequence(s) of the {a.workload} "
+                                       "shape, one per process"},
+            "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------------
+# clocks, peaks, ncu traffic
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.path = tempfile.mktemp(prefix="clk", suffix=".csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_uuid:
+            cmd += ["-i", gpu_uuid]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), float(parts[3]),
+                             parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[3] >= 50] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples_under_load": len(loaded), "samples": len(rows),
+                "power_w_max": max(r[2] for r in loaded)}
+
+
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "paged_fp8_speculative_gb300", "csrc", "*"))):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str) -> float | None:
+    """DRAM bytes per call from the committed ncu summary, if it matches the current sources."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        kv = {}
+        for line in open(path):
+            if ":" in line and line.lstrip().startswith("- "):
+                k, v = line.lstrip()[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("workload") == workload and kv.get("source_digest") == source_digest() and \
+                "dram_bytes_per_call" in kv:
+            return float(kv["dram_bytes_per_call"])
+    return None
+
+
+def workload_config(a) -> dict:
+    from paged_fp8_speculative_gb300 import synth
+    cfg = {"workload": a.workload}
+    shapes = {"verify_16x35k_gqa16": (16, 35000, 4, 16, 1), "verify_16x70k_gqa16": (16, 70000, 4, 16, 1),
+              "verify_16x35k_gqa8": (16, 35000, 4, 8, 1), "verify_4x35k_gqa16": (4, 35000, 4, 16, 1)}
+    if a.workload in shapes:
+        b, c, ql, hq, hkv = shapes[a.workload]
+        cfg.update(num_seqs=b, context=c, q_len=ql, num_q_heads=hq, num_kv_heads=hkv)
+    cfg.update(head_dim=256, page_size=16, kv="fp8 e4m3", q="bf16", out="bf16",
+               num_segments=a.segments if a.segments else "heuristic",
+               kv_replicas=a.replicas, l2="inputs larger than L2: rotating KV replicas, "
+               "randomly permuted page tables", parallelism=f"replicas x{a.gpus}")
+    return cfg
+
+
+# --------------------------------------------------------------------------------------------
+# our arm
+
+def run_ours(a) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu_base = cpu_baseline(a.workload)      # spawn pool, before any CUDA work
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    from paged_fp8_speculative_gb300 import api, synth
+
+    batch = synth.workload(a.workload, seed=1000 + rank, replicas=a.replicas, device="cuda")
+    tables = [batch.block_tables] + batch.replica_tables
+    R = len(tables)
+    S = a.segments or api.mtp_verify_attn_num_segments(batch.num_seqs, batch.num_kv_heads,
+                                                       batch.block_tables.shape[1])
+    kd = torch.tensor([batch.k_descale], dtype=torch.float32, device=dev)
+    vd = torch.tensor([batch.v_descale], dtype=torch.float32, device=dev)
+    ws = torch.empty(api.mtp_verify_attn_workspace_size(batch.total_q, batch.num_q_heads, S),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(batch.q)
+    stream = torch.cuda.current_stream()
+
+    def call(i, q=batch.q, bt=None, sl=batch.seq_lens, cu=batch.cu_seqlens_q):
+        api.mtp_verify_attn_fwd(q, batch.k_cache, batch.v_cache, tables[i % R] if bt is None else bt,
+                                sl, cu, kd, vd, batch.softmax_scale, num_segments=S, out=out,
+                                workspace=ws, stream=stream)
+
+    kv_bytes = batch.kv_bytes()
+    total_pages = sum((int(c) + 15) // 16 for c in batch.seq_lens.tolist())
+    alg_bytes = kv_bytes + 2 * batch.q.numel() * 2 + 4 * total_pages * batch.num_kv_heads
+
+    # streaming-read ceiling, in the same session
+    ceil_buf = torch.empty(int(a.ceiling_gib * (1 << 30)) // 16 * 16, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        api.mtpattn_stream_read(ceil_buf, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        api.mtpattn_stream_read(ceil_buf, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ceiling_gbs = 10 * ceil_buf.numel() / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del ceil_buf
+    torch.cuda.empty_cache()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+
+    # warm-up: W calls, and at least `warm_seconds` of calls
+    t_end = time.time() + a.warm_seconds
+    i = 0
+    while i < a.warmup or time.time() < t_end:
+        call(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+    # timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(a.steps):
+        call(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+
+    # end to end through the public API: host inputs in, host output back, every step
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_sl, h_cu = pin(batch.q), pin(batch.seq_lens), pin(batch.cu_seqlens_q)
+    h_bt = [pin(t) for t in tables]
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q, d_sl, d_cu = torch.empty_like(batch.q), torch.empty_like(batch.seq_lens), torch.empty_like(batch.cu_seqlens_q)
+    d_bt = torch.empty_like(tables[0])
+    h2d = h_q.numel() * 2 + h_sl.numel() * 4 + h_cu.numel() * 4 + h_bt[0].numel() * 4
+    d2h = h_out.numel() * 2
+
+    def e2e_step(i):
+        d_q.copy_(h_q, non_blocking=True)
+        d_bt.copy_(h_bt[i % R], non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        call(i, q=d_q, bt=d_bt, sl=d_sl, cu=d_cu)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(max(3, a.warmup // 4)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0.record(stream)
+    for i in range(a.steps):
+        e2e_step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = t0.elapsed_time(t1)
+
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    us_call = 1e3 * ms / a.steps
+    value = world * kv_bytes * a.steps / (ms * 1e-3) / 1e12
+    peak, peak_kind = hbm_peak()
+    achieved = alg_bytes / (us_call * 1e-6) / 1e9
+    traffic = ncu_traffic(a.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms / a.steps, "us_per_call": us_call,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic", "config": workload_config(a) | {"num_segments": S},
+        "frac_of_8tbs_nominal": value / world / 8.0,
+        "read_ceiling": {"value_gbs": ceiling_gbs, "frac": value / world * 1e3 / ceiling_gbs,
+                         "kernel": "mtpattn_stream_read, 16-B loads"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "mtp_verify_attn_fwd (main + reduce)",
+                     "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_call": alg_bytes},
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": world * kv_bytes * a.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": 1e3 * ms_e2e / a.steps},
+        "gpu_launches": 2 * a.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse_args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * mtpattn.h — C ABI of the paged fp8 split-KV attention library (libmtpattn.so)
+ * for the speculative-decoding verify, draft-extend and decode steps on GB300 (sm_103a).
+ *
+ * The operation.  Each sequence b has q_len_b query tokens (1..4, bf16,
+ * head_dim 256) packed at rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q, and
+ * seq_lens[b] keys in a paged NHD page-16 fp8 e4m3 K/V cache read in place
+ * through block_tables.  Query token t sees keys 0 .. seq_lens[b]-q_len_b+t
+ * (causal over the last q_len positions, bottom-right aligned); query head j
+ * reads KV head j / ratio with ratio = H_q / H_kv in {8, 16}; logits are
+ * softmax_scale * k_descale * <q, K>, the output is v_descale * softmax · V,
+ * rounded to bf16.  Sources: aiter PR #5190 page ("gfx950 assembly MTP-verify
+ * attention for head_dim 256 fp8 paged KV", Motivation, Modifications, Kernel
+ * notes, Supported) and SGLang PR #37465 page ("gfx950 assembly attention for
+ * EAGLE verify, draft extend and decode", Modifications: q_len 1..4 handled in
+ * one kernel for verify, draft extend and decode).  seq_lens counts the current
+ * query tokens (their K/V are already in the cache).
+ *
+ * Split-KV: the keys of each (sequence, KV head) are cut into num_segments
+ * segments of whole pages; a main kernel writes one partial output and one
+ * log-sum-exp per (row, segment) into the caller's workspace and a second
+ * kernel merges the segments by their LSE into the bf16 output (aiter PR #5190
+ * page, Modifications: "grid = segments x sequences x kv heads" and the
+ * split-KV segment reduce).  Empty segments are written neutrally, so any
+ * num_segments in [1, 64] gives the same result up to float32 re-association.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" must be CUDA device memory of the current device;
+ *    the library never dereferences them on the host, never allocates, never
+ *    synchronises and never copies device data to the host in mtp_verify_attn_fwd,
+ *    so a call may be captured in a CUDA graph.  The descales are read on the
+ *    device for the same reason (aiter PR #5190 page, Kernel notes).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - The caller owns every buffer.  The library keeps only a per-device cache
+ *    of the SM count.
+ *  - Return codes: MTPATTN_OK or a negative MTPATTN_E_*.  On an error return
+ *    nothing was launched.  Nothing prints, throws or traps.
+ */
+#ifndef MTPATTN_H
+#define MTPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MTPATTN_OK 0
+#define MTPATTN_E_ARG (-1)          /* null pointer, negative count, bad stride or alignment */
+#define MTPATTN_E_UNSUPPORTED (-2)  /* outside the envelope: head_dim, page size, ratio, segments */
+#define MTPATTN_E_DEVICE (-3)       /* a pointer is not device memory of the current device, or no device */
+#define MTPATTN_E_WORKSPACE (-4)    /* workspace null, too small or not 256-byte aligned */
+#define MTPATTN_E_LAUNCH (-5)       /* a kernel launch failed (cudaGetLastError after launch) */
+
+/* Device-side error bits OR-ed into the optional `status` word (device int32).
+ * The affected rows are written as zeros; nothing outside the given buffers is read. */
+#define MTPATTN_ERR_QLEN 1          /* q_len_b outside [1, 4] or cu_seqlens_q not ascending within total_q */
+#define MTPATTN_ERR_QLEN_GT_SEQ 2   /* q_len_b > seq_lens[b] */
+#define MTPATTN_ERR_PAGE 4          /* a block-table entry needed for a key is outside [0, num_pages) */
+#define MTPATTN_ERR_SEQ_TOO_LONG 8  /* seq_lens[b] > 16 * max_pages_per_seq */
+
+#define MTPATTN_HEAD_DIM 256
+#define MTPATTN_PAGE_SIZE 16
+#define MTPATTN_MAX_SEGMENTS 64
+#define MTPATTN_MAX_Q_LEN 4
+
+/*
+ * Number of KV segments per (sequence, KV head) for a batch shape, in [1, 64].
+ * Our reading of the pages' segment heuristic (aiter PR #5190 page,
+ * Modifications: mtp_verify_attn_num_segments(); the printed configurations
+ * fill the device exactly once): the largest S with S * num_seqs * num_kv_heads
+ * <= the SM count of `device`, clamped to [1, min(64, max_pages_per_seq)].
+ * device < 0 means the current device.  Returns a negative MTPATTN_E_* on bad
+ * arguments or when the device cannot be queried.
+ */
+int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
+                                     int32_t max_pages_per_seq, int32_t device);
+
+/*
+ * Bytes of device workspace mtp_verify_attn_fwd needs:
+ * float32 partial outputs [total_q * num_q_heads][num_segments][256] plus
+ * float32 partial log-sum-exps [total_q * num_q_heads][num_segments], each
+ * region 256-byte aligned.  Returns 0 for invalid arguments.
+ */
+size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int32_t num_segments);
+
+/*
+ * out = paged fp8 verify / draft-extend / decode attention (see the top of this file).
+ *
+ *  q            device bf16 [total_q][num_q_heads][256]; element strides q_stride_tok,
+ *               q_stride_head (multiples of 8), unit stride along head_dim; 16-byte aligned.
+ *  k_cache,     device e4m3 codes [num_pages][16][num_kv_heads][256], contiguous,
+ *  v_cache      16-byte aligned (NHD pages, read in place).
+ *  block_tables device int32 [num_seqs][max_pages_per_seq]; entries past
+ *               ceil(seq_lens[b]/16) are never read.
+ *  seq_lens     device int32 [num_seqs], keys per sequence including the query tokens.
+ *  cu_seqlens_q device int32 [num_seqs+1], cu[0] = 0, cu[num_seqs] = total_q, 1 <= q_len <= 4.
+ *  num_q_heads  = ratio * num_kv_heads with ratio 8 or 16.
+ *  k_descale,   device float32, one element each (per-tensor descales).
+ *  v_descale
+ *  softmax_scale  host float, multiplies the logits (usually 1/sqrt(256)).
+ *  num_segments in [1, 64], or 0 for mtp_verify_attn_num_segments().
+ *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned;
+ *               its contents on entry do not matter; calls that overlap on the GPU
+ *               must use different workspaces.
+ *  out          device bf16 [total_q][num_q_heads][256]; element strides out_stride_tok,
+ *               out_stride_head (multiples of 8), unit stride along head_dim.
+ *  status       optional device int32 (NULL = none); device-side MTPATTN_ERR_* bits are
+ *               OR-ed into it and never cleared by the library.
+ *  stream       cudaStream_t as void*.
+ * Two kernels are launched on `stream`: the split-KV main kernel and the segment reduce.
+ */
+int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                        const void* k_cache, const void* v_cache, int64_t num_pages,
+                        const int32_t* block_tables, int32_t max_pages_per_seq,
+                        const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                        int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                        int32_t num_kv_heads, const float* k_descale, const float* v_descale,
+                        float softmax_scale, int32_t num_segments,
+                        void* workspace, size_t workspace_bytes,
+                        void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                        int32_t* status, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mtp_verify_attn_strerror(int status);
+
+/*
+ * Streaming-read ceiling probe (the device's practical read bandwidth, measured
+ * the way the aiter PR #5190 page quotes its 5.9-6.9 TB/s ceiling): every byte
+ * of the device buffer `buf` (`bytes`, a multiple of 16, 16-byte aligned) is
+ * read once with 16-byte loads by `blocks` CTAs (0 = 4 per SM) and folded into
+ * one uint32 per CTA written to device `sink` [blocks], so the reads are not
+ * dead code.  One kernel launch on `stream`.
+ */
+int mtpattn_stream_read(const void* buf, size_t bytes, uint32_t* sink, int32_t blocks,
+                        void* stream);
+
+/* Number of CTAs mtpattn_stream_read launches for blocks = 0 on the current device. */
+int32_t mtpattn_stream_read_default_blocks(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTPATTN_H */

@@ -1,0 +1,53 @@
+"""ctypes loader for libmtpattn.so (the C ABI declared in include/mtpattn.h).
+
+There is no fallback: if the library is missing the import of this module's
+``lib()`` raises, so no caller can silently run anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmtpattn.so")
+
+_c_int, _c_i32, _c_i64, _c_size, _c_float = (ctypes.c_int, ctypes.c_int32, ctypes.c_int64,
+                                             ctypes.c_size_t, ctypes.c_float)
+_vp = ctypes.c_void_p
+
+# name -> (restype, argtypes), in the order of include/mtpattn.h
+SIGNATURES = {
+    "mtp_verify_attn_num_segments": (_c_i32, [_c_i32, _c_i32, _c_i32, _c_i32]),
+    "mtp_verify_attn_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32]),
+    "mtp_verify_attn_fwd": (_c_int, [
+        _vp, _c_i64, _c_i64,            # q, strides
+        _vp, _vp, _c_i64,               # k_cache, v_cache, num_pages
+        _vp, _c_i32,                    # block_tables, max_pages_per_seq
+        _vp, _vp,                       # seq_lens, cu_seqlens_q
+        _c_i32, _c_i32, _c_i32, _c_i32,  # num_seqs, total_q, num_q_heads, num_kv_heads
+        _vp, _vp, _c_float, _c_i32,     # k_descale, v_descale, softmax_scale, num_segments
+        _vp, _c_size,                   # workspace, workspace_bytes
+        _vp, _c_i64, _c_i64,            # out, strides
+        _vp, _vp]),                     # status, stream
+    "mtp_verify_attn_strerror": (ctypes.c_char_p, [_c_int]),
+    "mtpattn_stream_read": (_c_int, [_vp, _c_size, _vp, _c_i32, _vp]),
+    "mtpattn_stream_read_default_blocks": (_c_i32, []),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises RuntimeError if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_fp8_speculative_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB

@@ -1,0 +1,137 @@
+"""Python binding of the C ABI (argument marshalling only).
+
+Every function has the name of the C entry point it calls.  PyTorch supplies
+device memory and the current stream; every step of the computation runs in
+the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from ._lib import lib
+
+HEAD_DIM = 256
+PAGE_SIZE = 16
+MAX_SEGMENTS = 64
+
+OK, E_ARG, E_UNSUPPORTED, E_DEVICE, E_WORKSPACE, E_LAUNCH = 0, -1, -2, -3, -4, -5
+ERR_QLEN, ERR_QLEN_GT_SEQ, ERR_PAGE, ERR_SEQ_TOO_LONG = 1, 2, 4, 8
+
+
+class MtpAttnError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"mtpattn status {code}: {mtp_verify_attn_strerror(code)}")
+
+
+def mtp_verify_attn_strerror(code: int) -> str:
+    return lib().mtp_verify_attn_strerror(int(code)).decode()
+
+
+def mtp_verify_attn_num_segments(num_seqs: int, num_kv_heads: int, max_pages_per_seq: int,
+                                 device: int = -1) -> int:
+    r = lib().mtp_verify_attn_num_segments(num_seqs, num_kv_heads, max_pages_per_seq, device)
+    if r < 0:
+        raise MtpAttnError(r)
+    return r
+
+
+def mtp_verify_attn_workspace_size(total_q: int, num_q_heads: int, num_segments: int) -> int:
+    return int(lib().mtp_verify_attn_workspace_size(total_q, num_q_heads, num_segments))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _descale(x, device) -> torch.Tensor:
+    if isinstance(x, torch.Tensor):
+        return x
+    return torch.full((1,), float(x), dtype=torch.float32, device=device)
+
+
+def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                        cu_seqlens_q: torch.Tensor, k_descale, v_descale,
+                        softmax_scale: float, num_segments: Optional[int] = None,
+                        out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Paged fp8 verify / draft-extend / decode attention; returns ``out`` (bf16).
+
+    q [total_q, H_q, 256] bf16; k_cache / v_cache [num_pages, 16, H_kv, 256]
+    uint8 or float8_e4m3fn codes; block_tables [B, max_pages] int32; seq_lens [B]
+    int32; cu_seqlens_q [B+1] int32; descales 1-element float32 device tensors
+    (a Python float is copied to the device).  ``status`` is an optional int32
+    device word that collects device-side error bits (ERR_*).
+    """
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
+        raise ValueError("q must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
+    if k_cache.dtype not in (torch.uint8, torch.float8_e4m3fn) or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache / v_cache must be uint8 or float8_e4m3fn codes")
+    if k_cache.dim() != 4 or k_cache.shape[1] != PAGE_SIZE or k_cache.shape[3] != HEAD_DIM:
+        raise ValueError("k_cache must be [num_pages, 16, H_kv, 256]")
+    if v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or not v_cache.is_contiguous():
+        raise ValueError("k_cache and v_cache must be contiguous and of the same shape")
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("cu_seqlens_q", cu_seqlens_q)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    num_seqs = seq_lens.numel()
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or cu_seqlens_q.numel() != num_seqs + 1:
+        raise ValueError("block_tables [B, max_pages], seq_lens [B], cu_seqlens_q [B+1]")
+    total_q, hq, _ = q.shape
+    hkv = k_cache.shape[2]
+    dev = q.device
+    kd = _descale(k_descale, dev)
+    vd = _descale(v_descale, dev)
+    for name, t in (("k_descale", kd), ("v_descale", vd)):
+        if t.dtype != torch.float32 or t.numel() != 1:
+            raise ValueError(f"{name} must be a 1-element float32 tensor")
+    if num_segments is None or num_segments == 0:
+        num_segments = mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
+                                                    dev.index if dev.index is not None else -1)
+    if out is None:
+        out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM) or out.stride(2) != 1:
+        raise ValueError("out must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
+    need = mtp_verify_attn_workspace_size(total_q, hq, num_segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = lib().mtp_verify_attn_fwd(
+        _ptr(q), q.stride(0), q.stride(1),
+        _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), _ptr(cu_seqlens_q),
+        num_seqs, total_q, hq, hkv,
+        _ptr(kd), _ptr(vd), float(softmax_scale), int(num_segments),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), out.stride(0), out.stride(1),
+        _ptr(status), _stream_handle(stream))
+    if rc != OK:
+        raise MtpAttnError(rc)
+    return out
+
+
+def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, blocks: int = 0,
+                        stream=None) -> torch.Tensor:
+    """Read every byte of ``buf`` once (streaming-read ceiling probe); returns the sink."""
+    if blocks == 0:
+        blocks = int(lib().mtpattn_stream_read_default_blocks())
+        if blocks <= 0:
+            raise MtpAttnError(blocks)
+    if sink is None:
+        sink = torch.empty(blocks, dtype=torch.int32, device=buf.device)
+    nbytes = buf.numel() * buf.element_size()
+    rc = lib().mtpattn_stream_read(_ptr(buf), nbytes, _ptr(sink), blocks, _stream_handle(stream))
+    if rc != OK:
+        raise MtpAttnError(rc)
+    return sink

@@ -1,0 +1,78 @@
+// Split-KV segment reduce: merge the per-segment partial outputs of one query
+// row by their log-sum-exps and round to bf16 (the "split-KV segment reduce"
+// of the aiter PR #5190 page, Modifications).
+//
+//   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s
+//
+// Segments with lse = -inf (empty, or no visible key) get weight 0 without
+// ever forming (-inf) - (-inf).  A NaN lse marks a row the main kernel flagged
+// as invalid; such rows are written as zeros.  One warp per row, 8 dims per lane.
+#include "common.cuh"
+
+#include <math.h>
+
+namespace mtpattn {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+attn_reduce_kernel(const AttnParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
+  if (row >= rows) return;
+  const int S = p.num_segments;
+  const float* lse = p.lse_part + row * S;
+
+  // Each lane holds segments lane and lane + 32.
+  const float l0 = lane < S ? lse[lane] : -INFINITY;
+  const float l1 = lane + 32 < S ? lse[lane + 32] : -INFINITY;
+  int bad = isnan(l0) || isnan(l1);
+  float mx = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (!bad && mx != -INFINITY) {
+    const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
+    const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
+    const float* o = p.o_part + row * S * kHeadDim + lane * 8;
+    for (int s = 0; s < S; ++s) {
+      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      wsum += w;
+      if (w != 0.f) {
+        const float4 a = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim);
+        const float4 c = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim + 4);
+        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+        acc[4] = fmaf(w, c.x, acc[4]); acc[5] = fmaf(w, c.y, acc[5]);
+        acc[6] = fmaf(w, c.z, acc[6]); acc[7] = fmaf(w, c.w, acc[7]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t tok = row / p.num_q_heads, head = row - tok * p.num_q_heads;
+  __nv_bfloat16* dst = p.out + tok * p.out_stride_tok + head * p.out_stride_head + lane * 8;
+  uint32_t packed[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+    packed[j] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
+  const unsigned grid = static_cast<unsigned>((rows + kWarpsPerCta - 1) / kWarpsPerCta);
+  attn_reduce_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mtpattn

@@ -1,0 +1,64 @@
+// Shared definitions of the CUDA path (kernels and host launchers).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mtpattn.h"
+
+namespace mtpattn {
+
+constexpr int kHeadDim = MTPATTN_HEAD_DIM;    // 256
+constexpr int kPage = MTPATTN_PAGE_SIZE;      // 16 keys per page
+constexpr int kMaxQLen = MTPATTN_MAX_Q_LEN;   // 4
+constexpr int kMaxRows = 64;                  // q_len (<= 4) x ratio (<= 16) rows per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Everything one call needs on the device.  Strides are in elements.
+struct AttnParams {
+  const __nv_bfloat16* q;
+  int64_t q_stride_tok, q_stride_head;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  int64_t num_pages;
+  const int32_t* block_tables;
+  int32_t max_pages;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  int32_t num_seqs, total_q, num_q_heads, num_kv_heads, ratio;
+  const float* k_descale;
+  const float* v_descale;
+  float scale_log2;     // softmax_scale * log2(e): logits are kept in the log2 domain
+  int32_t num_segments;
+  float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
+  float* lse_part;      // [total_q * H_q][S] float32, log2-sum-exp2 of the segment (NaN = error)
+  __nv_bfloat16* out;
+  int64_t out_stride_tok, out_stride_head;
+  int32_t* status;      // optional
+};
+
+// Pages [begin, end) of segment s for a sequence of n_pages pages: equal shares of
+// ceil(n_pages / S) pages, the tail segments possibly short or empty.
+__host__ __device__ inline void segment_pages(int n_pages, int S, int s, int* begin, int* end) {
+  int pps = (n_pages + S - 1) / S;
+  int b = s * pps;
+  int e = b + pps;
+  if (b > n_pages) b = n_pages;
+  if (e > n_pages) e = n_pages;
+  *begin = b;
+  *end = e;
+}
+
+__device__ inline void set_status(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Host launchers (return cudaError_t of the launch).
+cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, int blocks,
+                               cudaStream_t stream);
+int device_sm_count(int device);
+
+}  // namespace mtpattn

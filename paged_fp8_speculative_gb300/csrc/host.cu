@@ -1,0 +1,202 @@
+// C-ABI entry points: argument checks, the segment heuristic, workspace
+// carving and the two launches.  Everything here runs on the host and never
+// touches device memory contents, so a call can be captured in a CUDA graph.
+#include "common.cuh"
+
+#include <math.h>
+#include <stddef.h>
+
+namespace mtpattn {
+
+int device_sm_count(int device) {
+  static int cache[64] = {0};
+  if (device < 0) {
+    if (cudaGetDevice(&device) != cudaSuccess) return -1;
+  }
+  if (device >= 64) return -1;
+  if (cache[device] > 0) return cache[device];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();
+    return -1;
+  }
+  cache[device] = sms;
+  return sms;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A pointer the kernels may dereference: device (or managed) memory of `device`.
+bool on_device(const void* ptr, int device) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return false;
+  return attr.device == device;
+}
+
+}  // namespace
+}  // namespace mtpattn
+
+using namespace mtpattn;
+
+extern "C" int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
+                                                int32_t max_pages_per_seq, int32_t device) {
+  if (num_seqs <= 0 || num_kv_heads <= 0 || max_pages_per_seq <= 0) return MTPATTN_E_ARG;
+  const int sms = device_sm_count(device);
+  if (sms <= 0) return MTPATTN_E_DEVICE;
+  const long long units = static_cast<long long>(num_seqs) * num_kv_heads;
+  long long s = sms / units;
+  if (s < 1) s = 1;
+  if (s > MTPATTN_MAX_SEGMENTS) s = MTPATTN_MAX_SEGMENTS;
+  if (s > max_pages_per_seq) s = max_pages_per_seq;
+  return static_cast<int32_t>(s);
+}
+
+extern "C" size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads,
+                                                 int32_t num_segments) {
+  if (total_q < 0 || num_q_heads <= 0 || num_segments < 1 ||
+      num_segments > MTPATTN_MAX_SEGMENTS)
+    return 0;
+  const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
+  const size_t lse = align_up(rows * num_segments * sizeof(float));
+  const size_t o = align_up(rows * num_segments * kHeadDim * sizeof(float));
+  return lse + o;
+}
+
+extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                                   const void* k_cache, const void* v_cache, int64_t num_pages,
+                                   const int32_t* block_tables, int32_t max_pages_per_seq,
+                                   const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                                   int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                   int32_t num_kv_heads, const float* k_descale,
+                                   const float* v_descale, float softmax_scale,
+                                   int32_t num_segments, void* workspace,
+                                   size_t workspace_bytes, void* out, int64_t out_stride_tok,
+                                   int64_t out_stride_head, int32_t* status, void* stream) {
+  // 1. plain argument checks
+  if (num_seqs < 0 || total_q < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
+      num_q_heads <= 0 || num_kv_heads <= 0)
+    return MTPATTN_E_ARG;
+  if (num_seqs == 0) return total_q == 0 ? MTPATTN_OK : MTPATTN_E_ARG;
+  if (total_q < num_seqs) return MTPATTN_E_ARG;          // every sequence has >= 1 query token
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seqlens_q ||
+      !k_descale || !v_descale || !out || num_pages == 0 || max_pages_per_seq == 0)
+    return MTPATTN_E_ARG;
+  if (!isfinite(softmax_scale)) return MTPATTN_E_ARG;
+  if (q_stride_tok <= 0 || q_stride_head <= 0 || out_stride_tok <= 0 || out_stride_head <= 0 ||
+      (q_stride_tok | q_stride_head | out_stride_tok | out_stride_head) % 8 != 0)
+    return MTPATTN_E_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(k_descale, 4) || !aligned(v_descale, 4) || !aligned(status, 4))
+    return MTPATTN_E_ARG;
+  // 2. the supported envelope
+  if (num_q_heads % num_kv_heads) return MTPATTN_E_UNSUPPORTED;
+  const int ratio = num_q_heads / num_kv_heads;
+  if (ratio != 8 && ratio != 16) return MTPATTN_E_UNSUPPORTED;
+  if (total_q > static_cast<int64_t>(num_seqs) * MTPATTN_MAX_Q_LEN) return MTPATTN_E_UNSUPPORTED;
+  if (num_segments < 0 || num_segments > MTPATTN_MAX_SEGMENTS) return MTPATTN_E_UNSUPPORTED;
+  // 3. the segment count (the heuristic needs the device) and the workspace
+  int device = -1;
+  if (num_segments == 0) {
+    if (cudaGetDevice(&device) != cudaSuccess) {
+      cudaGetLastError();
+      return MTPATTN_E_DEVICE;
+    }
+    num_segments = mtp_verify_attn_num_segments(num_seqs, num_kv_heads, max_pages_per_seq, device);
+    if (num_segments < 1) return MTPATTN_E_DEVICE;
+  }
+  const size_t need = mtp_verify_attn_workspace_size(total_q, num_q_heads, num_segments);
+  if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < need)
+    return MTPATTN_E_WORKSPACE;
+  // 4. every pointer must be memory the kernels can read on the current device
+  if (device < 0 && cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return MTPATTN_E_DEVICE;
+  }
+  const void* ptrs[] = {q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q,
+                        k_descale, v_descale, workspace, out};
+  for (const void* ptr : ptrs)
+    if (!on_device(ptr, device)) return MTPATTN_E_DEVICE;
+  if (status && !on_device(status, device)) return MTPATTN_E_DEVICE;
+
+  AttnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q_stride_tok = q_stride_tok;
+  p.q_stride_head = q_stride_head;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.num_pages = num_pages;
+  p.block_tables = block_tables;
+  p.max_pages = max_pages_per_seq;
+  p.seq_lens = seq_lens;
+  p.cu_q = cu_seqlens_q;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.ratio = ratio;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.num_segments = num_segments;
+  const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
+  p.lse_part = static_cast<float*>(workspace);
+  p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      align_up(rows * num_segments * sizeof(float)));
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out_stride_tok = out_stride_tok;
+  p.out_stride_head = out_stride_head;
+  p.status = status;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_attn_main(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
+  if (launch_attn_reduce(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
+  return MTPATTN_OK;
+}
+
+extern "C" const char* mtp_verify_attn_strerror(int status) {
+  switch (status) {
+    case MTPATTN_OK: return "ok";
+    case MTPATTN_E_ARG: return "invalid argument (null pointer, negative count, stride or alignment)";
+    case MTPATTN_E_UNSUPPORTED: return "unsupported configuration (GQA ratio must be 8 or 16, q_len <= 4, num_segments in [0, 64])";
+    case MTPATTN_E_DEVICE: return "pointer is not device memory of the current CUDA device, or no CUDA device";
+    case MTPATTN_E_WORKSPACE: return "workspace missing, smaller than mtp_verify_attn_workspace_size() or not 256-byte aligned";
+    case MTPATTN_E_LAUNCH: return "kernel launch failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int32_t mtpattn_stream_read_default_blocks(void) {
+  const int sms = device_sm_count(-1);
+  return sms > 0 ? 2 * sms : MTPATTN_E_DEVICE;
+}
+
+extern "C" int mtpattn_stream_read(const void* buf, size_t bytes, uint32_t* sink, int32_t blocks,
+                                   void* stream) {
+  if (!buf || !sink || blocks < 0 || bytes == 0 || bytes % 16 || !aligned(buf, 16) ||
+      !aligned(sink, 4))
+    return MTPATTN_E_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return MTPATTN_E_DEVICE;
+  }
+  if (blocks == 0) blocks = mtpattn_stream_read_default_blocks();
+  if (blocks <= 0) return MTPATTN_E_DEVICE;
+  if (!on_device(buf, device) || !on_device(sink, device)) return MTPATTN_E_DEVICE;
+  if (launch_stream_read(buf, bytes, sink, blocks, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MTPATTN_E_LAUNCH;
+  return MTPATTN_OK;
+}

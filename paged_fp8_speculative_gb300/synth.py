@@ -166,33 +166,33 @@ def make_batch(contexts: Sequence[int], q_lens: Sequence[int] | int, num_q_heads
                       float(v_descale), float(softmax_scale), num_kv_heads, page_size, tables[1:])
 
 
-# Named workloads (sizes as the benchmark configurations state them).
-def workload(name: str, *, seed: int = 0, replicas: int = 1, device: str = "cpu",
-             kv_recipe: str = "amax") -> PagedBatch:
+# Named workloads (sizes as the benchmark configurations state them):
+# name -> (contexts, q_lens, H_q, H_kv, k_descale, v_descale)
+def workload_spec(name: str):
     if name == "verify_tiny":            # 2 x 1000, q_len 4, 16/1, descales 1.0
-        return make_batch([1000, 1000], 4, 16, 1, seed=seed, replicas=replicas, device=device,
-                          kv_recipe=kv_recipe)
+        return [1000] * 2, [4] * 2, 16, 1, 1.0, 1.0
     if name == "verify_16x35k_gqa16":    # production verify shape
-        return make_batch([35000] * 16, 4, 16, 1, seed=seed, k_descale=0.5, v_descale=2.0,
-                          replicas=replicas, device=device, kv_recipe=kv_recipe)
+        return [35000] * 16, [4] * 16, 16, 1, 0.5, 2.0
     if name == "verify_16x70k_gqa16":
-        return make_batch([70000] * 16, 4, 16, 1, seed=seed, k_descale=0.5, v_descale=2.0,
-                          replicas=replicas, device=device, kv_recipe=kv_recipe)
+        return [70000] * 16, [4] * 16, 16, 1, 0.5, 2.0
     if name == "verify_2x777_kv2":       # 32 q heads on 2 KV heads
-        return make_batch([777, 777], 4, 32, 2, seed=seed, replicas=replicas, device=device,
-                          kv_recipe=kv_recipe)
+        return [777] * 2, [4] * 2, 32, 2, 1.0, 1.0
     if name == "verify_16x35k_gqa8":
-        return make_batch([35000] * 16, 4, 8, 1, seed=seed, k_descale=0.5, v_descale=2.0,
-                          replicas=replicas, device=device, kv_recipe=kv_recipe)
+        return [35000] * 16, [4] * 16, 8, 1, 0.5, 2.0
     if name == "verify_4x35k_gqa16":     # run with num_segments 64
-        return make_batch([35000] * 4, 4, 16, 1, seed=seed, k_descale=0.5, v_descale=2.0,
-                          replicas=replicas, device=device, kv_recipe=kv_recipe)
+        return [35000] * 4, [4] * 4, 16, 1, 0.5, 2.0
     if name in ("draft_extend_8", "decode_8"):
         ctx = log_uniform_contexts(8, 6, 105000, seed=4000)
-        ql = uniform_q_lens(8, 1, 4, seed=4001) if name == "draft_extend_8" else 1
-        return make_batch(ctx, ql, 16, 1, seed=seed, k_descale=0.5, v_descale=2.0,
-                          replicas=replicas, device=device, kv_recipe=kv_recipe)
+        ql = uniform_q_lens(8, 1, 4, seed=4001) if name == "draft_extend_8" else [1] * 8
+        return ctx, ql, 16, 1, 0.5, 2.0
     raise KeyError(name)
+
+
+def workload(name: str, *, seed: int = 0, replicas: int = 1, device: str = "cpu",
+             kv_recipe: str = "amax") -> PagedBatch:
+    ctx, ql, hq, hkv, kd, vd = workload_spec(name)
+    return make_batch(ctx, ql, hq, hkv, seed=seed, k_descale=kd, v_descale=vd,
+                      replicas=replicas, device=device, kv_recipe=kv_recipe)
 
 
 WORKLOADS = ("verify_tiny", "verify_16x35k_gqa16", "verify_16x70k_gqa16", "verify_2x777_kv2",

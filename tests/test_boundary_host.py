@@ -1,0 +1,128 @@
+"""Host-only tests of the C ABI (no GPU): the library loads, exports exactly what
+include/mtpattn.h declares, sizes the workspace, and refuses bad arguments with
+the documented status codes before it touches any device state."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_fp8_speculative_gb300 import _lib, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mtpattn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**([A-Za-z_]\w*)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert set(names) == set(_lib.SIGNATURES), names
+    assert "mtp_verify_attn_fwd" in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5):
+        assert api.mtp_verify_attn_strerror(code) not in ("", "unknown status")
+    assert api.mtp_verify_attn_strerror(-99) == "unknown status"
+
+
+def test_workspace_size():
+    f = api.mtp_verify_attn_workspace_size
+    rows = 64 * 16
+    lse = (rows * 16 * 4 + 255) // 256 * 256
+    assert f(64, 16, 16) == lse + rows * 16 * 256 * 4
+    assert f(7, 8, 3) == ((7 * 8 * 3 * 4 + 255) // 256 * 256) + ((7 * 8 * 3 * 1024 + 255) // 256 * 256)
+    assert f(64, 16, 0) == 0 and f(64, 16, 65) == 0 and f(-1, 16, 4) == 0 and f(4, 0, 4) == 0
+
+
+# A call whose every argument is valid on the host side; pointers are fake but
+# aligned and are never dereferenced before the device checks.
+FAKE = 0x10000
+
+
+def good_args(**over):
+    a = dict(q=FAKE, q_st=16 * 256, q_sh=256, k=FAKE, v=FAKE, num_pages=10, bt=FAKE, max_pages=5,
+             sl=FAKE, cu=FAKE, num_seqs=2, total_q=8, hq=16, hkv=1, kd=FAKE, vd=FAKE, scale=0.0625,
+             S=4, ws=FAKE, ws_bytes=1 << 30, out=FAKE, o_st=16 * 256, o_sh=256, status=None,
+             stream=None)
+    a.update(over)
+    return a
+
+
+def call(a):
+    return _lib.lib().mtp_verify_attn_fwd(
+        a["q"], a["q_st"], a["q_sh"], a["k"], a["v"], a["num_pages"], a["bt"], a["max_pages"],
+        a["sl"], a["cu"], a["num_seqs"], a["total_q"], a["hq"], a["hkv"], a["kd"], a["vd"],
+        a["scale"], a["S"], a["ws"], a["ws_bytes"], a["out"], a["o_st"], a["o_sh"], a["status"],
+        a["stream"])
+
+
+REFUSALS = [
+    (dict(q=None), api.E_ARG),
+    (dict(k=None), api.E_ARG),
+    (dict(bt=None), api.E_ARG),
+    (dict(kd=None), api.E_ARG),
+    (dict(out=None), api.E_ARG),
+    (dict(num_seqs=-1), api.E_ARG),
+    (dict(total_q=1), api.E_ARG),                     # fewer query tokens than sequences
+    (dict(num_pages=0), api.E_ARG),
+    (dict(max_pages=0), api.E_ARG),
+    (dict(q_sh=100), api.E_ARG),                      # stride not a multiple of 8 elements
+    (dict(o_st=0), api.E_ARG),
+    (dict(q=FAKE + 8), api.E_ARG),                    # not 16-byte aligned
+    (dict(scale=float("nan")), api.E_ARG),
+    (dict(hkv=0), api.E_ARG),
+    (dict(hq=12, hkv=1), api.E_UNSUPPORTED),          # ratio 12
+    (dict(hq=32, hkv=1), api.E_UNSUPPORTED),          # ratio 32
+    (dict(hq=16, hkv=3), api.E_UNSUPPORTED),          # not a multiple
+    (dict(total_q=9), api.E_UNSUPPORTED),             # q_len > 4 somewhere
+    (dict(S=65), api.E_UNSUPPORTED),
+    (dict(S=-2), api.E_UNSUPPORTED),
+    (dict(ws=None), api.E_WORKSPACE),
+    (dict(ws=FAKE + 16), api.E_WORKSPACE),            # not 256-byte aligned
+    (dict(ws_bytes=1000), api.E_WORKSPACE),
+]
+
+
+@pytest.mark.parametrize("over,code", REFUSALS)
+def test_refusals_before_any_launch(over, code):
+    assert call(good_args(**over)) == code
+
+
+def test_empty_batch_is_a_no_op():
+    assert call(good_args(num_seqs=0, total_q=0)) == api.OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_is_reported():
+    assert call(good_args()) == api.E_DEVICE
+    assert _lib.lib().mtp_verify_attn_num_segments(16, 1, 100, -1) == api.E_DEVICE
+    assert _lib.lib().mtpattn_stream_read(FAKE, 1024, FAKE, 4, None) == api.E_DEVICE
+
+
+def test_num_segments_argument_checks():
+    f = _lib.lib().mtp_verify_attn_num_segments
+    assert f(0, 1, 10, -1) == api.E_ARG
+    assert f(4, 0, 10, -1) == api.E_ARG
+    assert f(4, 1, 0, -1) == api.E_ARG
+
+
+def test_stream_read_argument_checks():
+    f = _lib.lib().mtpattn_stream_read
+    assert f(None, 1024, FAKE, 4, None) == api.E_ARG
+    assert f(FAKE, 1000, FAKE, 4, None) == api.E_ARG       # not a multiple of 16
+    assert f(FAKE, 1024, None, 4, None) == api.E_ARG

@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance.  The method's stated bound is max|gpu - oracle| / std(out) <= 0.01
+for a kernel that keeps Q and P in bf16/fp32 precision.  The output itself is
+bf16, and rounding the exact value to bf16 alone costs up to half a bf16 ulp
+(2^-8 of the leading power of two), which for the largest outputs of a
+Gaussian-like output tensor is 0.008-0.016 std.  So each element is granted
+half a bf16 ulp of the exact value on top of the 0.01 std budget
+(oracle.excess_over_half_ulp).  Index and page handling is checked bit-exactly
+through segment-count invariance on data whose result does not depend on the
+summation order.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_fp8_speculative_gb300 import api, synth
+from tests.helpers import oracle_args
+
+pytestmark = pytest.mark.gpu
+
+TOL = 0.01
+
+
+def run_gpu(batch, num_segments=None, status=None, block_tables=None, out=None, q=None):
+    d = batch
+    kd = torch.tensor([d.k_descale], dtype=torch.float32, device="cuda")
+    vd = torch.tensor([d.v_descale], dtype=torch.float32, device="cuda")
+    o = api.mtp_verify_attn_fwd(d.q if q is None else q, d.k_cache, d.v_cache,
+                                d.block_tables if block_tables is None else block_tables,
+                                d.seq_lens, d.cu_seqlens_q, kd, vd, d.softmax_scale,
+                                num_segments=num_segments, status=status, out=out)
+    torch.cuda.synchronize()
+    return o
+
+
+def check(batch, num_segments=None, tol=TOL):
+    gb = batch.to("cuda")
+    got = run_gpu(gb, num_segments).float().cpu().numpy().astype(np.float64)
+    ref = oracle.verify_attention(*oracle_args(batch))
+    err = oracle.excess_over_half_ulp(got, ref)
+    raw = oracle.max_err_over_std(got, ref)
+    assert np.isfinite(got).all()
+    assert err <= tol, f"excess error {err:.4g} std (raw {raw:.4g})"
+    return err, raw
+
+
+CASES = {
+    # the configurations' small parity shapes
+    "tiny_2x1000_gqa16": lambda: synth.workload("verify_tiny", seed=1),
+    "tiny_unit_recipe": lambda: synth.workload("verify_tiny", seed=2, kv_recipe="unit"),
+    "tiny_descales": lambda: synth.make_batch([1000, 1000], 4, 16, 1, seed=3, k_descale=0.5,
+                                              v_descale=2.0),
+    "gqa8": lambda: synth.make_batch([1000, 1000], 4, 8, 1, seed=4),
+    "kv2_777": lambda: synth.workload("verify_2x777_kv2", seed=5),
+    "3x8000": lambda: synth.make_batch([8000] * 3, 4, 16, 1, seed=6),
+    # ragged draft extend and q_len 1 decode over a context mix with a partial last page
+    "ragged_extend": lambda: synth.make_batch([6, 17, 250, 1031, 4099, 33], [1, 4, 2, 3, 4, 1],
+                                              16, 1, seed=7, k_descale=0.5, v_descale=2.0),
+    "decode": lambda: synth.make_batch([6, 17, 250, 1031, 4099, 33], 1, 16, 1, seed=8,
+                                       k_descale=0.5, v_descale=2.0),
+    "ragged_gqa8_kv2": lambda: synth.make_batch([4, 40, 300, 1500], [4, 1, 3, 2], 16, 2, seed=9),
+    "tiny_contexts": lambda: synth.make_batch([1, 2, 3, 4, 5, 16, 17], [1, 1, 2, 4, 4, 3, 1],
+                                              16, 1, seed=10, kv_recipe="unit"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_parity_against_oracle(name):
+    check(CASES[name]())
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 16, 63, 64])
+def test_any_segment_count_matches_oracle(S):
+    check(synth.make_batch([1000, 345, 80], [4, 2, 3], 16, 1, seed=20 + S, k_descale=0.5,
+                           v_descale=2.0), num_segments=S)
+
+
+def test_segment_count_invariance_uniform_keys():
+    """All keys equal => the exact output is the mean of the visible V rows.  Every
+    segment count must give the same result up to float32 re-association; a
+    missed or double-counted page would move it by far more."""
+    batch = synth.make_batch([1000, 345, 80, 17], [4, 2, 3, 1], 16, 1, seed=30, kv_recipe="unit")
+    batch.k_cache.fill_(0x38)
+    ref = oracle.verify_attention(*oracle_args(batch))
+    gb = batch.to("cuda")
+    outs = []
+    for S in (1, 2, 4, 7, 16, 33, 64):
+        o = run_gpu(gb, S).float().cpu().numpy()
+        assert oracle.excess_over_half_ulp(o, ref) <= 1e-3
+        outs.append(o)
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 2 ** -6 * np.abs(outs[0]).max()
+
+
+def test_underflow_spike_closed_form():
+    """q[0] = 8, K_0[0] = 14, V_0 = +1, every other V = -1 over 16384 keys:
+    exact out = (e^7 - 16383) / (e^7 + 16383) = -0.874524 in every coordinate."""
+    n, D = 16384, 256
+    k = torch.zeros(n // 16, 16, 1, D, dtype=torch.uint8)
+    k[0, 0, 0, 0] = 0x56
+    v = torch.full((n // 16, 16, 1, D), 0xB8, dtype=torch.uint8)
+    v[0, 0, 0, :] = 0x38
+    q = torch.zeros(1, 16, D, dtype=torch.bfloat16)
+    q[0, :, 0] = 8.0
+    bt = torch.randperm(n // 16, dtype=torch.int32)[None]
+    kc = torch.empty_like(k); vc = torch.empty_like(v)
+    kc[bt[0].long()] = k; vc[bt[0].long()] = v
+    batch = synth.PagedBatch(q, kc, vc, bt, torch.tensor([n], dtype=torch.int32),
+                             torch.tensor([0, 1], dtype=torch.int32), 1.0, 1.0, 1.0 / 16, 1, 16)
+    expect = (math.exp(7) - (n - 1)) / (math.exp(7) + (n - 1))
+    for S in (1, 16, 64):
+        o = run_gpu(batch.to("cuda"), S).float().cpu().numpy()
+        assert np.abs(o - expect).max() <= 2 ** -8
+
+
+def test_strided_q_and_out_views():
+    batch = synth.make_batch([300, 700], [3, 4], 16, 1, seed=40)
+    ref = oracle.verify_attention(*oracle_args(batch))
+    gb = batch.to("cuda")
+    big_q = torch.zeros(gb.total_q, 3 * 16, 256, dtype=torch.bfloat16, device="cuda")
+    big_q[:, 16:32] = gb.q                               # q as a slice of a fused projection
+    big_o = torch.zeros(gb.total_q, 2, 16, 256, dtype=torch.bfloat16, device="cuda")
+    out = big_o[:, 1]
+    run_gpu(gb, 4, q=big_q[:, 16:32], out=out)
+    assert oracle.excess_over_half_ulp(out.float().cpu().numpy(), ref) <= TOL
+    assert big_o[:, 0].abs().max().item() == 0
+
+
+def test_repeatable_and_graph_replay_bit_identical():
+    batch = synth.make_batch([5000, 2000], 4, 16, 1, seed=50).to("cuda")
+    kd = torch.tensor([batch.k_descale], device="cuda")
+    vd = torch.tensor([batch.v_descale], device="cuda")
+    S = 8
+    ws = torch.empty(api.mtp_verify_attn_workspace_size(batch.total_q, 16, S), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(batch.q)
+    args = (batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+            batch.cu_seqlens_q, kd, vd, batch.softmax_scale)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        api.mtp_verify_attn_fwd(*args, num_segments=S, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    api.mtp_verify_attn_fwd(*args, num_segments=S, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g, stream=s):
+        api.mtp_verify_attn_fwd(*args, num_segments=S, out=out, workspace=ws, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    # descales are read on the device at replay time
+    kd.fill_(batch.k_descale * 2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert not torch.equal(out, eager)
+
+
+def test_device_errors_set_status_and_zero_rows():
+    batch = synth.make_batch([100, 200, 64], [4, 4, 2], 16, 1, seed=60).to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = run_gpu(batch, 4, status=status)
+    assert status.item() == 0
+    # q_len > seq_len for sequence 2
+    bad = synth.PagedBatch(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                           torch.tensor([100, 200, 1], dtype=torch.int32, device="cuda"),
+                           batch.cu_seqlens_q, batch.k_descale, batch.v_descale,
+                           batch.softmax_scale, 1, 16)
+    o2 = run_gpu(bad, 4, status=status)
+    assert status.item() & api.ERR_QLEN_GT_SEQ
+    assert o2[8:].abs().max().item() == 0
+    assert torch.equal(o2[:8], o[:8])
+    # a block-table entry outside the pool for sequence 1
+    status.zero_()
+    bt = batch.block_tables.clone()
+    bt[1, 3] = batch.k_cache.shape[0] + 5
+    o3 = run_gpu(batch, 4, status=status, block_tables=bt)
+    assert status.item() & api.ERR_PAGE
+    assert o3[4:8].abs().max().item() == 0
+    assert torch.equal(o3[:4], o[:4]) and torch.equal(o3[8:], o[8:])
+
+
+def test_host_pointers_are_refused():
+    batch = synth.make_batch([100], 4, 16, 1, seed=70)
+    gb = batch.to("cuda")
+    with pytest.raises(api.MtpAttnError) as ei:
+        api.mtp_verify_attn_fwd(gb.q, gb.k_cache, gb.v_cache, batch.block_tables, gb.seq_lens,
+                                gb.cu_seqlens_q, torch.ones(1, device="cuda"),
+                                torch.ones(1, device="cuda"), 0.0625, num_segments=2)
+    assert ei.value.code == api.E_DEVICE
+
+
+def test_num_segments_heuristic_on_device():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = api.mtp_verify_attn_num_segments(16, 1, 2188)
+    assert 1 <= s <= 64 and s * 16 <= max(sms, 16)
+    assert api.mtp_verify_attn_num_segments(1, 1, 3) == 3
+    assert api.mtp_verify_attn_num_segments(1000, 8, 100) == 1
+
+
+@pytest.mark.parametrize("name,S", [("verify_16x35k_gqa16", 16), ("verify_16x35k_gqa8", 16),
+                                    ("verify_4x35k_gqa16", 64), ("verify_16x70k_gqa16", 16),
+                                    ("draft_extend_8", 0), ("decode_8", 0)])
+def test_full_size_sampled_against_oracle(name, S):
+    """The benchmark shapes at full size, in the launch configuration the bench
+    times, checked on sampled sequences the oracle computes one by one."""
+    batch = synth.workload(name, seed=1, device="cuda")
+    got = run_gpu(batch, S or None).float().cpu().numpy().astype(np.float64)
+    args = oracle_args(batch)
+    B = batch.num_seqs
+    seqs = sorted({0, B - 1, B // 2})
+    rows = oracle.verify_attention_rows(*args, seqs=seqs)
+    cu = batch.cu_seqlens_q.cpu().tolist()
+    ref = np.concatenate([rows[b] for b in seqs])
+    res = np.concatenate([got[cu[b]:cu[b + 1]] for b in seqs])
+    assert oracle.excess_over_half_ulp(res, ref) <= TOL
