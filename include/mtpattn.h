@@ -52,6 +52,7 @@ extern "C" {
 #define MTPATTN_E_DEVICE (-3)       /* a pointer is not device memory of the current device, or no device */
 #define MTPATTN_E_WORKSPACE (-4)    /* workspace null, too small or not 256-byte aligned */
 #define MTPATTN_E_LAUNCH (-5)       /* a kernel launch failed (cudaGetLastError after launch) */
+#define MTPATTN_E_SCRATCH_LIMIT (-6) /* the call needs more than MTPATTN_STATIC_SCRATCH_BYTES of scratch */
 
 /* Device-side error bits OR-ed into the optional `status` word (device int32).
  * The affected rows are written as zeros; nothing outside the given buffers is read. */
@@ -121,6 +122,44 @@ int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_he
                         void* workspace, size_t workspace_bytes,
                         void* out, int64_t out_stride_tok, int64_t out_stride_head,
                         int32_t* status, void* stream);
+
+/*
+ * Size of the library-owned device scratch array used by
+ * mtp_verify_attn_fwd_static_scratch: 32 MiB, held on every GPU that loads the
+ * library until the process exits.
+ */
+#define MTPATTN_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * mtp_verify_attn_fwd without a caller workspace, for callers that cannot
+ * allocate device memory: code inside another framework's memory pool that may
+ * not call cudaMalloc, launches issued while a CUDA graph is being captured
+ * (a fresh cudaMalloc is not allowed there), or latency-critical loops that
+ * must not reach cudaMalloc / cudaFree because those can synchronise the device.
+ * The pages have no counterpart of this entry point.
+ *
+ * Arguments are those of mtp_verify_attn_fwd minus workspace / workspace_bytes;
+ * the caller still passes every input and the output.  The split-KV partials go
+ * to a file-scope device array of MTPATTN_STATIC_SCRATCH_BYTES that the library
+ * owns; it allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * Calls needing more scratch than that (mtp_verify_attn_workspace_size() of the
+ * resolved segment count) return MTPATTN_E_SCRATCH_LIMIT and launch nothing.
+ * The first call on each device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents, so calls that overlap on the GPU (other streams, other threads) race
+ * on it and must be serialised by the caller.  Other return codes and the device
+ * status bits are those of mtp_verify_attn_fwd.
+ */
+int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                                       const void* k_cache, const void* v_cache, int64_t num_pages,
+                                       const int32_t* block_tables, int32_t max_pages_per_seq,
+                                       const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                                       int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                       int32_t num_kv_heads, const float* k_descale,
+                                       const float* v_descale, float softmax_scale,
+                                       int32_t num_segments, void* out, int64_t out_stride_tok,
+                                       int64_t out_stride_head, int32_t* status, void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* mtp_verify_attn_strerror(int status);

@@ -17,6 +17,8 @@ PAGE_SIZE = 16
 MAX_SEGMENTS = 64
 
 OK, E_ARG, E_UNSUPPORTED, E_DEVICE, E_WORKSPACE, E_LAUNCH = 0, -1, -2, -3, -4, -5
+E_SCRATCH_LIMIT = -6
+STATIC_SCRATCH_BYTES = 32 << 20
 ERR_QLEN, ERR_QLEN_GT_SEQ, ERR_PAGE, ERR_SEQ_TOO_LONG = 1, 2, 4, 8
 
 
@@ -114,6 +116,34 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
         num_seqs, total_q, hq, hkv,
         _ptr(kd), _ptr(vd), float(softmax_scale), int(num_segments),
         _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), out.stride(0), out.stride(1),
+        _ptr(status), _stream_handle(stream))
+    if rc != OK:
+        raise MtpAttnError(rc)
+    return out
+
+
+def mtp_verify_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor,
+                                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                       seq_lens: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                                       k_descale: torch.Tensor, v_descale: torch.Tensor,
+                                       softmax_scale: float, num_segments: int, out: torch.Tensor,
+                                       status: Optional[torch.Tensor] = None,
+                                       stream=None) -> torch.Tensor:
+    """The attention without a caller workspace, for callers that cannot allocate.
+
+    The split-KV partials go to the library's own static device array
+    (STATIC_SCRATCH_BYTES per GPU), so this wrapper allocates nothing either:
+    ``out``, the descale tensors and every input are the caller's.  Calls that
+    overlap on the GPU share that array and race; serialise them.
+    """
+    rc = lib().mtp_verify_attn_fwd_static_scratch(
+        _ptr(q), q.stride(0), q.stride(1),
+        _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), _ptr(cu_seqlens_q),
+        seq_lens.numel(), q.shape[0], q.shape[1], k_cache.shape[2],
+        _ptr(k_descale), _ptr(v_descale), float(softmax_scale), int(num_segments),
         _ptr(out), out.stride(0), out.stride(1),
         _ptr(status), _stream_handle(stream))
     if rc != OK:

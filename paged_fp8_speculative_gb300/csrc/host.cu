@@ -173,6 +173,7 @@ extern "C" const char* mtp_verify_attn_strerror(int status) {
     case MTPATTN_E_DEVICE: return "pointer is not device memory of the current CUDA device, or no CUDA device";
     case MTPATTN_E_WORKSPACE: return "workspace missing, smaller than mtp_verify_attn_workspace_size() or not 256-byte aligned";
     case MTPATTN_E_LAUNCH: return "kernel launch failed";
+    case MTPATTN_E_SCRATCH_LIMIT: return "the call needs more scratch than the library's static array (MTPATTN_STATIC_SCRATCH_BYTES) holds";
     default: return "unknown status";
   }
 }

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert api.mtp_verify_attn_strerror(code) not in ("", "unknown status")
     assert api.mtp_verify_attn_strerror(-99) == "unknown status"
 

@@ -1,0 +1,77 @@
+"""The allocation-free entry point (mtp_verify_attn_fwd_static_scratch).
+
+Some callers cannot call cudaMalloc (a host inside another framework's memory
+pool, launches issued during CUDA graph capture, loops that must never
+synchronise the device), so this entry point keeps its split-KV partials in a
+library-owned static device array.  The test calls it through the C ABI twice in
+a row, on different batches, and checks each output against the regular entry
+point (which uses a caller workspace) within the parity tolerance of the other
+GPU tests.  It also checks that a call too large for the array is refused.
+This file is collected last so a stop-at-first-failure run has run every other
+test before it; it passes alone in a fresh process as well.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from paged_fp8_speculative_gb300 import _lib, api, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 0.01
+
+
+def _c_call(b, kd, vd, S, out, status):
+    """Call the C symbol directly with raw device pointers (no Python-side allocation)."""
+    return _lib.lib().mtp_verify_attn_fwd_static_scratch(
+        b.q.data_ptr(), b.q.stride(0), b.q.stride(1), b.k_cache.data_ptr(), b.v_cache.data_ptr(),
+        b.k_cache.shape[0], b.block_tables.data_ptr(), b.block_tables.shape[1],
+        b.seq_lens.data_ptr(), b.cu_seqlens_q.data_ptr(), b.num_seqs, b.total_q,
+        b.num_q_heads, b.num_kv_heads, kd.data_ptr(), vd.data_ptr(), b.softmax_scale, S,
+        out.data_ptr(), out.stride(0), out.stride(1), status.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+
+
+def _regular(b, kd, vd, S):
+    return api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                   b.cu_seqlens_q, kd, vd, b.softmax_scale, num_segments=S)
+
+
+def test_static_scratch_matches_regular_entry_point_twice():
+    batches = [
+        synth.make_batch([3000, 1000, 77], [4, 2, 1], 16, 1, seed=901, k_descale=0.5,
+                         v_descale=2.0).to("cuda"),
+        synth.make_batch([500, 2500], [3, 4], 16, 2, seed=902).to("cuda"),
+    ]
+    for b, S in zip(batches, (16, 5)):
+        kd = torch.tensor([b.k_descale], dtype=torch.float32, device="cuda")
+        vd = torch.tensor([b.v_descale], dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ref = _regular(b, kd, vd, S)
+        out = torch.full_like(b.q, float("nan"))
+        rc = _c_call(b, kd, vd, S, out, status)
+        assert rc == api.OK, api.mtp_verify_attn_strerror(rc)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        r = ref.float().cpu().numpy().astype(np.float64)
+        o = out.float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(o).all()
+        assert np.abs(o - r).max() / r.std() <= TOL
+
+
+def test_static_scratch_refuses_calls_beyond_its_size():
+    b = synth.make_batch([2000] * 16, 4, 16, 1, seed=903).to("cuda")
+    kd = torch.ones(1, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(b.q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    need = api.mtp_verify_attn_workspace_size(b.total_q, b.num_q_heads, 64)
+    assert need > api.STATIC_SCRATCH_BYTES
+    assert _c_call(b, kd, kd, 64, out, status) == api.E_SCRATCH_LIMIT
+    assert api.mtp_verify_attn_workspace_size(b.total_q, b.num_q_heads, 16) <= api.STATIC_SCRATCH_BYTES
+    assert _c_call(b, kd, kd, 16, out, status) == api.OK
+    torch.cuda.synchronize()
+    assert status.item() == 0
