@@ -60,6 +60,8 @@ extern "C" {
 #define MTPATTN_ERR_QLEN_GT_SEQ 2   /* q_len_b > seq_lens[b] */
 #define MTPATTN_ERR_PAGE 4          /* a block-table entry needed for a key is outside [0, num_pages) */
 #define MTPATTN_ERR_SEQ_TOO_LONG 8  /* seq_lens[b] > 16 * max_pages_per_seq */
+#define MTPATTN_ERR_TIMEOUT 16      /* a pipeline wait inside the main kernel gave up (about 2 s
+                                       without progress); that call's output is not valid */
 
 #define MTPATTN_HEAD_DIM 256
 #define MTPATTN_PAGE_SIZE 16

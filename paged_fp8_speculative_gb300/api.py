@@ -19,7 +19,7 @@ MAX_SEGMENTS = 64
 OK, E_ARG, E_UNSUPPORTED, E_DEVICE, E_WORKSPACE, E_LAUNCH = 0, -1, -2, -3, -4, -5
 E_SCRATCH_LIMIT = -6
 STATIC_SCRATCH_BYTES = 32 << 20
-ERR_QLEN, ERR_QLEN_GT_SEQ, ERR_PAGE, ERR_SEQ_TOO_LONG = 1, 2, 4, 8
+ERR_QLEN, ERR_QLEN_GT_SEQ, ERR_PAGE, ERR_SEQ_TOO_LONG, ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class MtpAttnError(RuntimeError):

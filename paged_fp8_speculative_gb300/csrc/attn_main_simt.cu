@@ -268,7 +268,7 @@ attn_main_simt_kernel(const AttnParams p) {
 
 }  // namespace
 
-cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_attn_main_simt(const AttnParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(Smem);
   cudaError_t e = cudaFuncSetAttribute(attn_main_simt_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
