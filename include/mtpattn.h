@@ -16,13 +16,15 @@
  * one kernel for verify, draft extend and decode).  seq_lens counts the current
  * query tokens (their K/V are already in the cache).
  *
- * Split-KV: the keys of each (sequence, KV head) are cut into num_segments
- * segments of whole pages; a main kernel writes one partial output and one
- * log-sum-exp per (row, segment) into the caller's workspace and a second
- * kernel merges the segments by their LSE into the bf16 output (aiter PR #5190
- * page, Modifications: "grid = segments x sequences x kv heads" and the
- * split-KV segment reduce).  Empty segments are written neutrally, so any
- * num_segments in [1, 64] gives the same result up to float32 re-association.
+ * Split-KV: the keys of each (sequence, KV head) are cut into pieces of whole
+ * pages; a main kernel writes one partial output and one log-sum-exp per (row,
+ * piece) into the caller's workspace and a second kernel merges them by their
+ * LSE into the bf16 output (aiter PR #5190 page, Modifications: the split-KV
+ * main kernel and its segment reduce).  num_segments (S) is the number of split
+ * slots per (sequence, KV head): the pages of all units are shared out in equal
+ * chunks over the SMs, no unit is cut into more than S pieces, and slots a unit
+ * does not use are written empty.  Any S in [1, 64] gives the same result up to
+ * float32 re-association; S = 1 keeps every unit whole.
  *
  * Conventions for every entry point:
  *  - Pointers marked "device" must be CUDA device memory of the current device;
@@ -69,13 +71,13 @@ extern "C" {
 #define MTPATTN_MAX_Q_LEN 4
 
 /*
- * Number of KV segments per (sequence, KV head) for a batch shape, in [1, 64].
- * Our reading of the pages' segment heuristic (aiter PR #5190 page,
- * Modifications: mtp_verify_attn_num_segments(); the printed configurations
- * fill the device exactly once): the largest S with S * num_seqs * num_kv_heads
- * <= the SM count of `device`, clamped to [1, min(64, max_pages_per_seq)].
- * device < 0 means the current device.  Returns a negative MTPATTN_E_* on bad
- * arguments or when the device cannot be queried.
+ * Number of split slots S per (sequence, KV head) for a batch shape, in [1, 64]
+ * (aiter PR #5190 page, Modifications: mtp_verify_attn_num_segments(); no
+ * formula is printed).  Our rule: the page share of one SM is
+ * ceil(num_seqs * num_kv_heads * max_pages_per_seq / SMs); S is the number of
+ * shares a full-length unit can touch, ceil(max_pages_per_seq / share) + 1,
+ * capped at 64.  device < 0 means the current device.  Returns a negative
+ * MTPATTN_E_* on bad arguments or when the device cannot be queried.
  */
 int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
                                      int32_t max_pages_per_seq, int32_t device);

@@ -1,30 +1,43 @@
 // Split-KV main kernel on the sm_100-family tensor cores (tcgen05, TMA, TMEM).
 //
-// Work items are the (segment s, sequence b, KV head h) triples of the aiter
-// PR #5190 page's decomposition ("grid = segments x sequences x kv heads");
-// here a persistent grid of one CTA per SM walks them, so the K/V stream of the
-// next item starts while the current one finishes.
+// Scheduling.  The pages' kernel runs one work-group per (segment, sequence,
+// KV head) (aiter PR #5190 page, Modifications: "grid = segments x sequences x
+// kv heads").  Here every (sequence b, KV head h) unit owns max_pages_per_seq
+// slots of a virtual page line, and a persistent grid of one CTA per SM cuts
+// that line into equal chunks of C pages, so every SM streams the same number
+// of pages.  The part of a unit inside one chunk is a "piece"; it writes its
+// partial output into split slot (chunk - first chunk of the unit).  C is at
+// least max_pages / (S - 1), so a unit never has more than S pieces, and the
+// unit's last piece marks its unused slots empty (lse = -inf).  With S = 1,
+// C = max_pages: one piece per unit.
 //
-// Roles (192 threads):
-//   warp 0   producer: TMA loads of the item's K and V pages, straight from the
-//            paged NHD cache through the block table (two 128-byte-wide boxes
-//            per page, 128B-swizzled), into 3-stage K and V rings;
-//   warp 1   MMA issuer (one thread) and TMEM owner;
-//   warps 2-5  softmax group, one TMEM lane each: Q preparation, online
-//            softmax, O rescale and the segment epilogue.
+// Roles (352 threads):
+//   warps 0, 10  producers of K (warp 0) and V (warp 10): TMA loads of the
+//              item's pages, straight from the paged NHD cache through the
+//              block table (two 128-byte-wide boxes per page, 128B-swizzled),
+//              into 3-stage K and V rings.  K and V run independently because
+//              a V slot frees one tile later than a K slot;
+//   warp 1     MMA issuer (one thread) and TMEM owner;
+//   warps 2-9  softmax: two groups of four warps.  Each group covers all 128
+//              TMEM lanes; group 0 owns key columns 0-63 of every tile (and O
+//              columns 0-127), group 1 key columns 64-127 (O columns 128-255).
 //
 // Precision.  Both contractions run as e4m3 x e4m3 -> f32 MMAs on the cache
-// bytes themselves, so K and V are never converted.  To keep Q and P at bf16
-// precision, each is written as the sum of two e4m3 terms:
+// bytes themselves, so K and V are never converted.  Q and P keep bf16-class
+// precision by writing each as the sum of two e4m3 terms:
 //   Q:  x = q * 2^a (a per row, so max|x| is in [128, 256)),
 //       hi = e4m3(x), lo = e4m3((x - hi) * 16);  x = hi + lo/16 exactly for
 //       every element within 2^-13 of the row maximum (a bf16 value has 8
-//       significant bits, hi keeps 4 and the remainder fits lo's 4);
-//   P:  p * 256 = hi + lo/16 the same way, p in [0, 1].
+//       significant bits: hi keeps 4 and the remainder fits lo's 4);
+//   P:  p_s = 2^(s - m + 8 - kTau) in [0, 256] as hi + lo/16 the same way.
 // The hi and lo rows are stacked into one M = 128 MMA: TMEM lane 32w + t holds
 // hi (t < 16) or lo (t >= 16) of query row 16w + (t & 15), so the two halves
-// of a row live in lanes t and t ^ 16 of the same warp and are added with one
-// shuffle.  S = hi + lo/16 per tile; O = (O_hi + O_lo/16) / 256 at the end.
+// of a row sit in lanes t and t ^ 16 of one warp and are added with one
+// shuffle: S = hi + lo/16 per tile, O = O_hi + O_lo/16 at the end.
+//
+// Online softmax with a lazy reference: m is only raised (and O rescaled in
+// TMEM) when a tile's row maximum exceeds it by more than kTau (log2 units);
+// otherwise p <= 2^kTau, which the P encoding scale 2^(8 - kTau) absorbs.
 //
 // Tile = 128 keys (8 pages).  TMEM: S double buffer at columns 0 and 128 (the
 // tile's P overwrites the first 32 columns of its S buffer, 4 e4m3 per column),
@@ -42,7 +55,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kTileKeys = 128;
 constexpr int kPagesPerTile = kTileKeys / kPage;       // 8
 constexpr int kHalfBytes = kTileKeys * 128;            // one 128-byte column half of a tile
@@ -52,42 +66,78 @@ constexpr int kQBytes = 128 * 256;                     // stacked hi/lo Q, two h
 constexpr int kSCols = 128;
 constexpr int kOCol = 256;
 constexpr int kTmemCols = 512;
+constexpr float kTau = 3.f;                            // lazy-rescale threshold (log2 units)
+constexpr float kPShift = 8.f - kTau;                  // p_s = p * 2^kPShift <= 256
 
-// Shared-memory map (offsets from a 1024-byte-aligned base).
+// Shared-memory map (offsets from a 1024-byte-aligned base).  The whole 227 KB
+// is requested; the kernel checks that the aligned layout fits before using it.
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;       // + barriers + alignment slack
+constexpr int kOffXchg = kOffBar + 256;                // 2 x 2 x 128 floats of cross-group exchange
+constexpr int kLayoutBytes = kOffXchg + 2 * 2 * 128 * 4;
+constexpr int kSmemBytes = 232448;
+static_assert(kLayoutBytes + 512 <= kSmemBytes, "shared-memory layout");
 
 struct TcParams {
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   AttnParams a;
-  int32_t num_items;
+  int64_t chunk_pages;   // C
+  int64_t num_chunks;    // ceil(units * max_pages / C)
 };
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_ready, final_mma;
+  uint64_t xbar[2];                 // cross-group exchange, one per slot parity
   uint32_t tmem_base;
   int32_t abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-// Geometry of one work item, computed identically by every role.
-struct Item {
-  int s, b, h, L, q0, ql, R, pb, pe, ntiles, err;
+// Position in this CTA's walk: chunk k and unit u (unit = h * num_seqs + b).
+struct Cursor {
+  int64_t k, u;
 };
 
-__device__ __forceinline__ Item item_info(const AttnParams& p, int it, int lane) {
+__device__ __forceinline__ Cursor cursor_first(const TcParams& prm) {
+  Cursor c;
+  c.k = blockIdx.x;
+  c.u = c.k * prm.chunk_pages / prm.a.max_pages;
+  return c;
+}
+__device__ __forceinline__ Cursor cursor_next(const TcParams& prm, Cursor c) {
+  const int64_t V = prm.a.max_pages;
+  const int64_t end = min((c.k + 1) * prm.chunk_pages,
+                          static_cast<int64_t>(prm.a.num_seqs) * prm.a.num_kv_heads * V);
+  ++c.u;
+  if (c.u * V >= end) {
+    c.k += gridDim.x;
+    c.u = c.k * prm.chunk_pages / V;
+  }
+  return c;
+}
+
+// Geometry of one piece, computed identically by every role.
+struct Item {
+  int s, b, h, L, q0, ql, R, pb, pe, ntiles, err;
+  bool last;   // the unit's last piece: it also marks the unit's unused slots empty
+};
+
+__device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, int lane) {
+  const AttnParams& p = prm.a;
   Item x;
-  const int S = p.num_segments;
-  x.s = it % S;
-  const int rest = it / S;
-  x.b = rest % p.num_seqs;
-  x.h = rest / p.num_seqs;
+  const int64_t V = p.max_pages, C = prm.chunk_pages;
+  const int64_t k_first = c.u * V / C;
+  x.s = static_cast<int>(c.k - k_first);
+  x.last = c.k == (c.u * V + V - 1) / C;
+  x.b = static_cast<int>(c.u % p.num_seqs);
+  x.h = static_cast<int>(c.u / p.num_seqs);
+  const int64_t vp0 = max(c.k * C, c.u * V) - c.u * V;         // virtual page range of the piece
+  const int64_t vp1 = min((c.k + 1) * C, (c.u + 1) * V) - c.u * V;
   x.L = p.seq_lens[x.b];
   x.q0 = p.cu_q[x.b];
   const int q1 = p.cu_q[x.b + 1];
@@ -100,7 +150,11 @@ __device__ __forceinline__ Item item_info(const AttnParams& p, int it, int lane)
   if (!x.err && n_pages > p.max_pages) x.err |= MTPATTN_ERR_SEQ_TOO_LONG;
   x.R = rows_known ? x.ql * p.ratio : 0;
   x.pb = x.pe = 0;
-  if (!x.err) segment_pages(n_pages, S, x.s, &x.pb, &x.pe);
+  if (!x.err) {
+    x.pb = static_cast<int>(vp0);
+    x.pe = static_cast<int>(min(vp1, static_cast<int64_t>(n_pages)));
+    if (x.pe < x.pb) x.pe = x.pb;
+  }
   if (!x.err && x.pe > x.pb) {
     const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
     int bad = 0;
@@ -141,13 +195,44 @@ __device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, u
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
   return __int_as_float((e + 127) << 23);
 }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 c;
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rc, ra, rb;\n mov.b64 {%0, %1}, rc;\n}\n"
+      : "=f"(c.x), "=f"(c.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return c;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 c;
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rc, ra, rb;\n mov.b64 {%0, %1}, rc;\n}\n"
+      : "=f"(c.x), "=f"(c.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return c;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {  // a * b + c
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (rel. err ~2^-22)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  if (base + kLayoutBytes > smem_raw + kSmemBytes) {     // uniform across the CTA
+    if (threadIdx.x == 0) set_status(prm.a.status, MTPATTN_ERR_TIMEOUT);
+    return;
+  }
   Bars& bars = *reinterpret_cast<Bars*>(base + kOffBar);
+  float* xchg = reinterpret_cast<float*>(base + kOffXchg);   // [parity][group][128 lanes]
   const AttnParams& p = prm.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &bars.abort;
@@ -166,11 +251,13 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i]), 128);
+      mbar_init(smem_u32(&bars.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars.q_ready), 128);
+    mbar_init(smem_u32(&bars.q_ready), kSoftmaxThreads);
     mbar_init(smem_u32(&bars.final_mma), 1);
+    mbar_init(smem_u32(&bars.xbar[0]), kSoftmaxThreads);
+    mbar_init(smem_u32(&bars.xbar[1]), kSoftmaxThreads);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -183,54 +270,43 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 0) {
-    // ======================================= producer ===========================================
-    if (lane == 0) {
-      prefetch_tmap(&prm.tmap_k);
-      prefetch_tmap(&prm.tmap_v);
-    }
+  if (warp == 0 || warp == 10) {
+    // ================================ producers (K: warp 0, V: warp 10) ============================
+    const bool is_v = warp == 10;
+    const CUtensorMap* map = is_v ? &prm.tmap_v : &prm.tmap_k;
+    uint64_t* full = is_v ? bars.v_full : bars.k_full;
+    uint64_t* empty = is_v ? bars.v_empty : bars.k_empty;
+    const int ring = is_v ? kOffV : kOffK;
+    if (lane == 0) prefetch_tmap(map);
     const uint64_t pol = l2_policy_evict_first();
     uint32_t t = 0;  // global tile counter
-    for (int it = blockIdx.x; it < prm.num_items && !*abort_flag; it += gridDim.x) {
-      const Item x = item_info(p, it, lane);
+    for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
+      const Item x = item_info(prm, cur, lane);
       if (lane == 0) {
         const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
         for (int j = 0; j < x.ntiles; ++j, ++t) {
           const int pg0 = x.pb + j * kPagesPerTile;
           const int np = min(kPagesPerTile, x.pe - pg0);
           const int st = t % kStages;
-          const uint32_t ph = ((t / kStages) & 1) ^ 1;
-          if (!mbar_wait(smem_u32(&bars.k_empty[st]), ph, abort_flag)) break;
-          const uint32_t kf = smem_u32(&bars.k_full[st]);
-          mbar_arrive_expect_tx(kf, np * 2 * 2048);
-          const uint32_t kdst = smem_u32(base + kOffK + st * kTileBytes);
+          if (!mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag)) break;
+          const uint32_t fb = smem_u32(&full[st]);
+          mbar_arrive_expect_tx(fb, np * 2 * 2048);
+          const uint32_t dst = smem_u32(base + ring + st * kTileBytes);
           for (int i = 0; i < np; ++i) {
             const int phys = bt[pg0 + i];
-            tma_load_4d(kdst + i * 2048, &prm.tmap_k, kf, 0, x.h, 0, phys, pol);
-            tma_load_4d(kdst + kHalfBytes + i * 2048, &prm.tmap_k, kf, 128, x.h, 0, phys, pol);
-          }
-          if (!mbar_wait(smem_u32(&bars.v_empty[st]), ph, abort_flag)) break;
-          const uint32_t vf = smem_u32(&bars.v_full[st]);
-          mbar_arrive_expect_tx(vf, np * 2 * 2048);
-          const uint32_t vdst = smem_u32(base + kOffV + st * kTileBytes);
-          for (int i = 0; i < np; ++i) {
-            const int phys = bt[pg0 + i];
-            tma_load_4d(vdst + i * 2048, &prm.tmap_v, vf, 0, x.h, 0, phys, pol);
-            tma_load_4d(vdst + kHalfBytes + i * 2048, &prm.tmap_v, vf, 128, x.h, 0, phys, pol);
+            tma_load_4d(dst + i * 2048, map, fb, 0, x.h, 0, phys, pol);
+            tma_load_4d(dst + kHalfBytes + i * 2048, map, fb, 128, x.h, 0, phys, pol);
           }
         }
       }
       t = __shfl_sync(0xffffffffu, t, 0);
     }
-    // Never leave with copies in flight: wait for the last issued tiles of both rings.
+    // Never leave with copies in flight: wait for the last issued tiles of the ring.
     if (lane == 0) {
       for (uint32_t k = 0; k < kStages && k < t; ++k) {
         const uint32_t u = t - 1 - k;
-        const uint32_t ph = (u / kStages) & 1;
         volatile int no_abort = 0;
-        mbar_wait(smem_u32(&bars.k_full[u % kStages]), ph, &no_abort);
-        no_abort = 0;
-        mbar_wait(smem_u32(&bars.v_full[u % kStages]), ph, &no_abort);
+        mbar_wait(smem_u32(&full[u % kStages]), (u / kStages) & 1, &no_abort);
       }
     }
   } else if (warp == 1) {
@@ -240,8 +316,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     const uint32_t q_addr = smem_u32(base + kOffQ);
     uint32_t t = 0;
     uint32_t items_run = 0;
-    for (int it = blockIdx.x; it < prm.num_items && !*abort_flag; it += gridDim.x) {
-      const Item x = item_info(p, it, lane);
+    for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
+      const Item x = item_info(prm, cur, lane);
       if (x.ntiles == 0) continue;
       if (lane == 0) {
         bool ok = mbar_wait(smem_u32(&bars.q_ready), items_run & 1, abort_flag);
@@ -291,202 +367,297 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       mbar_wait(smem_u32(&bars.final_mma), 0, &no_abort);
     }
   } else {
-    // ======================================= softmax group =======================================
-    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-    const bool is_hi = lane < 16;
-    const int rloc = 16 * quad + (lane & 15);  // query row of this lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+    // ======================================= softmax warps =======================================
+    // Warp (quadrant q, half g) owns TMEM lanes 32q + 16g .. +15: query rows r = 16q + 8g + a
+    // (a < 8), hi in lane 32q + 16g + a and lo 8 lanes below.  With the 16x256b access shape
+    // thread t holds both lanes of row a = t/4 for the column pairs 8j + 2(t%4) (+1), so the
+    // hi + lo/16 sum is local and a row max takes two shuffles.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int c4 = lane & 3;
+    const int arow = lane >> 2;
+    const int rloc = 16 * quad + 8 * half + arow;           // query row of this thread
+    const uint32_t blk_addr = tmem + (static_cast<uint32_t>(32 * quad + 16 * half) << 16);
+    // Q preparation writes A row 32q + lane, half `half` of its 256 bytes.
+    const int L32 = 32 * quad + lane;
+    const bool q_is_hi = (lane & 15) < 8;
+    const int q_row = 16 * quad + 8 * (lane >> 4) + (lane & 7);
     const float kd = __ldg(p.k_descale);
     const float vd = __ldg(p.v_descale);
-    uint32_t t = 0;
-    for (int it = blockIdx.x; it < prm.num_items && !*abort_flag; it += gridDim.x) {
-      const Item x = item_info(p, it, lane);
-      const bool row_valid = rloc < x.R;
-      if (x.err) {
-        if (is_hi && row_valid)
-          p.lse_part[out_row(p, x, rloc) * p.num_segments + x.s] = __int_as_float(0x7fc00000);
-        if (lane == 0 && warp == 2) set_status(p.status, x.err);
-        continue;
-      }
-      if (x.ntiles == 0) {
-        if (row_valid) {
-          float* o = p.o_part + (out_row(p, x, rloc) * p.num_segments + x.s) * kHeadDim + (is_hi ? 0 : 128);
-          for (int d = 0; d < 128; d += 4) *reinterpret_cast<float4*>(o + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (is_hi) p.lse_part[out_row(p, x, rloc) * p.num_segments + x.s] = -INFINITY;
-        }
-        continue;
-      }
+    const bool even = (c4 & 1) == 0;                         // even: writes P_hi of the row
+    const uint32_t sel_lo = even ? 0x5410u : 0x1054u;        // byte selectors of the P words
+    const uint32_t sel_hi = even ? 0x7632u : 0x3276u;
 
-      // ---- Q: scale the row to [128, 256), split into hi / lo e4m3, write the stacked tile --
+    // The unit's unused split slots (after its last piece) are empty: lse = -inf, and the
+    // reduce never reads the partial output of a slot whose weight is 0.
+    auto close_unit = [&](const Item& y) {
+      if (y.last && c4 == 0 && rloc < y.R)
+        for (int s2 = y.s + 1; s2 < p.num_segments; ++s2)
+          p.lse_part[out_row(p, y, rloc) * p.num_segments + s2] = -INFINITY;
+    };
+    // Pieces with nothing to compute: an error gets a NaN LSE (the reduce writes zeros),
+    // an empty piece an empty slot.
+    auto trivial_item = [&](const Item& y) {
+      if (c4 == 0 && rloc < y.R)
+        p.lse_part[out_row(p, y, rloc) * p.num_segments + y.s] =
+            y.err ? __int_as_float(0x7fc00000) : -INFINITY;
+      if (y.err && lane == 0 && warp == 2) set_status(p.status, y.err);
+      close_unit(y);
+    };
+    // First piece with tiles at or after cursor c (finishing trivial pieces on the way).
+    auto next_running = [&](Cursor c, Item& y) -> Cursor {
+      for (; c.k < prm.num_chunks; c = cursor_next(prm, c)) {
+        y = item_info(prm, c, lane);
+        if (y.ntiles > 0) return c;
+        trivial_item(y);
+      }
+      return c;
+    };
+    // Q of piece y into the stacked A tile: this thread writes bytes half*128 .. +127 of
+    // A row L32.  The row's scale 2^a (max |q| * 2^a in [128, 256)) needs the max over
+    // both halves: the other half of row L32 is in warp (quad, half ^ 1), lane `lane`,
+    // exchanged through shared memory and the q_ready-independent xbar barriers.
+    int xpar = 0;
+    uint32_t xphase = 0;
+    auto exchange = [&](float v, float& other) -> bool {
+      xchg[(xpar * 2 + half) * 128 + L32] = v;
+      mbar_arrive(smem_u32(&bars.xbar[xpar]));
+      const bool ok = __all_sync(0xffffffffu,
+                                 mbar_wait(smem_u32(&bars.xbar[xpar]), (xphase >> xpar) & 1, abort_flag));
+      other = xchg[(xpar * 2 + (half ^ 1)) * 128 + L32];
+      xphase ^= 1u << xpar;
+      xpar ^= 1;
+      return ok;
+    };
+    auto prepare_q = [&](const Item& y, int& a_exp_row) -> bool {
       int a_exp = 0;
-      {
-        const int L32 = 32 * quad + lane;      // A-tile row == TMEM lane
-        unsigned char* qrow = base + kOffQ + L32 * 128;
-        const __nv_bfloat16* src = nullptr;
-        float mx = 0.f;
-        if (row_valid) {
-          const int tk = rloc / p.ratio, g = rloc - tk * p.ratio;
-          src = p.q + static_cast<int64_t>(x.q0 + tk) * p.q_stride_tok +
-                static_cast<int64_t>(x.h * p.ratio + g) * p.q_stride_head;
-          for (int c = 0; c < kHeadDim; c += 8) {
-            const uint4 w = *reinterpret_cast<const uint4*>(src + c);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      const bool valid = q_row < y.R;
+      uint4 w[16];                               // all 16 loads in flight at once
+      float mx = 0.f;
+      if (valid) {
+        const int tk = q_row / p.ratio, g = q_row - tk * p.ratio;
+        const __nv_bfloat16* src = p.q + static_cast<int64_t>(y.q0 + tk) * p.q_stride_tok +
+                                   static_cast<int64_t>(y.h * p.ratio + g) * p.q_stride_head +
+                                   half * 128;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              mx = fmaxf(mx, fabsf(__uint_as_float(ww[k] << 16)));
-              mx = fmaxf(mx, fabsf(__uint_as_float(ww[k] & 0xFFFF0000u)));
-            }
-          }
-          if (mx > 0.f) {
-            int e;
-            frexpf(mx, &e);                      // mx = f * 2^e, f in [0.5, 1)
-            a_exp = min(126, max(-126, 8 - e));  // mx * 2^a in [128, 256)
+        for (int c = 0; c < 16; ++c) w[c] = *reinterpret_cast<const uint4*>(src + 8 * c);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(ww[k] << 16)),
+                                 fabsf(__uint_as_float(ww[k] & 0xFFFF0000u))));
+        }
+      }
+      float mx_other;
+      if (!exchange(mx, mx_other)) return false;
+      mx = fmaxf(mx, mx_other);
+      if (mx > 0.f) {
+        int e;
+        frexpf(mx, &e);                          // mx = f * 2^e, f in [0.5, 1)
+        a_exp = min(126, max(-126, 8 - e));      // mx * 2^a in [128, 256)
+      }
+      const float sc = pow2f(a_exp);
+      unsigned char* qrow = base + kOffQ + half * (kQBytes / 2) + L32 * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {              // 8 output chunks of 16 codes
+        uint32_t out[4] = {0u, 0u, 0u, 0u};
+        if (valid) {
+          const uint32_t ww[8] = {w[2 * c].x, w[2 * c].y, w[2 * c].z, w[2 * c].w,
+                                  w[2 * c + 1].x, w[2 * c + 1].y, w[2 * c + 1].z, w[2 * c + 1].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t a0 = ww[2 * k], a1 = ww[2 * k + 1];
+            uint32_t hi, lo;
+            split4(__uint_as_float(a0 << 16) * sc, __uint_as_float(a0 & 0xFFFF0000u) * sc,
+                   __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc, hi, lo);
+            out[k] = q_is_hi ? hi : lo;
           }
         }
-        const float sc = pow2f(a_exp);
-#pragma unroll 1
-        for (int c = 0; c < 16; ++c) {           // 16 output chunks of 16 codes
-          uint32_t out[4] = {0u, 0u, 0u, 0u};
-          if (row_valid) {
-            const uint4 w0 = *reinterpret_cast<const uint4*>(src + 16 * c);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16 * c + 8);
-            const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t a0 = ww[2 * k], a1 = ww[2 * k + 1];
-              uint32_t hi, lo;
-              split4(__uint_as_float(a0 << 16) * sc, __uint_as_float(a0 & 0xFFFF0000u) * sc,
-                     __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc, hi, lo);
-              out[k] = is_hi ? hi : lo;
-            }
-          }
-          const int half = c >> 3, chunk = c & 7;
-          *reinterpret_cast<uint4*>(qrow + half * (kQBytes / 2) + ((chunk ^ (L32 & 7)) * 16)) =
-              make_uint4(out[0], out[1], out[2], out[3]);
-        }
+        *reinterpret_cast<uint4*>(qrow + ((c ^ (L32 & 7)) * 16)) = make_uint4(out[0], out[1], out[2], out[3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.q_ready));
+      // this thread's softmax row (rloc) is A rows 32q+16g+a / +8: lane 16g + a of this warp
+      a_exp_row = __shfl_sync(0xffffffffu, a_exp, 16 * half + arow);
+      return true;
+    };
 
+    uint32_t t = 0;
+    Item x;
+    Cursor it = next_running(cursor_first(prm), x);
+    int a_exp = 0;
+    bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp);
+    while (alive && it.k < prm.num_chunks) {
+      const bool row_valid = rloc < x.R;
+      const bool warp_active = __any_sync(0xffffffffu, row_valid);
       const int tk = row_valid ? rloc / p.ratio : 0;
-      // last visible key of this row, clipped to the segment's pages
+      // last visible key of this row, clipped to the piece's pages
       const int vis_max = row_valid ? min(x.L - x.ql + tk, x.pe * kPage - 1) : -1;
       const float sscale = p.scale_log2 * kd * pow2f(-a_exp);
-      float m_run = -INFINITY, l_part = 0.f;
+      const float2 w_hi = make_float2(sscale, sscale);
+      const float2 w_lo = make_float2(sscale * 0.0625f, sscale * 0.0625f);
+      float m_ref = -INFINITY, l_part = 0.f;
+      Item xn;                                 // next piece, looked up during the last tile
+      Cursor itn;
+      itn.k = prm.num_chunks;
+      itn.u = 0;
+      int a_next = 0;
 
       for (int j = 0; j < x.ntiles; ++j) {
         const uint32_t u = t + j;
         const uint32_t sb = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[sb]), (u >> 1) & 1, abort_flag))) break;
+        if (j == x.ntiles - 1) {
+          itn = cursor_next(prm, it);
+          if (itn.k < prm.num_chunks) xn = item_info(prm, itn, lane);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[sb]), (u >> 1) & 1, abort_flag))) { alive = false; break; }
         tc_fence_after();
-        const int key0 = (x.pb + j * kPagesPerTile) * kPage + (is_hi ? 0 : 16);
-        float s[64];
+        float s[32];                           // s[2jj + e]: key 8jj + 2 c4 + e of the tile
+        float alpha = 1.f;
+        bool rescale = false;
+        uint32_t pw[16];
+        if (warp_active) {
+          uint32_t v0[32], v1[32];
+          tmem_ld16x256_x8(blk_addr + sb * kSCols, v0);
+          tmem_ld16x256_x8(blk_addr + sb * kSCols + 64, v1);
+          tmem_ld_wait(v0);
+          tmem_ld_wait(v1);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + sb * kSCols + 32 * c, v);
-          tmem_ld_wait(v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float mine = __uint_as_float(is_hi ? v[i] : v[16 + i]);
-            const float send = __uint_as_float(is_hi ? v[16 + i] : v[i]);
-            const float other = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float comb = is_hi ? fmaf(other, 0.0625f, mine) : fmaf(mine, 0.0625f, other);
-            const int key = key0 + 32 * c + i;
-            s[16 * c + i] = key <= vis_max ? comb * sscale : -INFINITY;
+          for (int jj = 0; jj < 8; ++jj) {
+            const float2 h0 = make_float2(__uint_as_float(v0[4 * jj]), __uint_as_float(v0[4 * jj + 1]));
+            const float2 l0 = make_float2(__uint_as_float(v0[4 * jj + 2]), __uint_as_float(v0[4 * jj + 3]));
+            const float2 h1 = make_float2(__uint_as_float(v1[4 * jj]), __uint_as_float(v1[4 * jj + 1]));
+            const float2 l1 = make_float2(__uint_as_float(v1[4 * jj + 2]), __uint_as_float(v1[4 * jj + 3]));
+            const float2 c0 = ffma2(l0, w_lo, fmul2(h0, w_hi));
+            const float2 c1 = ffma2(l1, w_lo, fmul2(h1, w_hi));
+            s[2 * jj] = c0.x; s[2 * jj + 1] = c0.y;
+            s[16 + 2 * jj] = c1.x; s[17 + 2 * jj] = c1.y;
           }
+          const int key0 = (x.pb + j * kPagesPerTile) * kPage + 2 * c4;
+          if (!__all_sync(0xffffffffu, key0 - 2 * c4 + kTileKeys - 1 <= vis_max)) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (key0 + 8 * (i >> 1) + (i & 1) > vis_max) s[i] = -INFINITY;
+          }
+          float m8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m8[i] = fmaxf(m8[i], m8[i + 4]);
+          float mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          // lazy reference: raise m only when the tile beats it by more than kTau
+          if (mx != -INFINITY && (m_ref == -INFINITY || mx > m_ref + kTau)) {
+            if (m_ref != -INFINITY) {
+              alpha = ex2(m_ref - mx);
+              rescale = true;
+            }
+            m_ref = mx;
+          }
+          const float2 moff = make_float2(kPShift - m_ref, kPShift - m_ref);  // p_s = 2^(s - m + shift)
+          uint32_t hiw[8], low[8];
+          float2 ps2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            // s[2k], s[2k+1]: keys of column pair jj = k (first 64 keys) ... packed per split4 as
+            // (jj = 2m, 2m+1) so each word's halves are two consecutive pairs.
+            const int i0 = (k < 4) ? 4 * k : 16 + 4 * (k - 4);
+            const float2 e01 = fadd2(make_float2(s[i0], s[i0 + 1]), moff);
+            const float2 e23 = fadd2(make_float2(s[i0 + 2], s[i0 + 3]), moff);
+            const float2 p01 = make_float2(ex2(e01.x), ex2(e01.y));   // s = -inf gives 0
+            const float2 p23 = make_float2(ex2(e23.x), ex2(e23.y));
+            ps2 = fadd2(ps2, fadd2(p01, p23));
+            split4(p01.x, p01.y, p23.x, p23.y, hiw[k], low[k]);
+          }
+          l_part = l_part * alpha + (ps2.x + ps2.y);
+          // P words: word of pair jj (keys 8jj + 4(c4>>1) .. +3) is built by the even/odd thread
+          // pair c4, c4^1: even keeps its hi bytes and takes the partner's, odd likewise for lo.
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t own = even ? hiw[k] : low[k];
+            const uint32_t snd = even ? low[k] : hiw[k];
+            const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, 1);
+            pw[2 * k] = __byte_perm(own, rcv, sel_lo);
+            pw[2 * k + 1] = __byte_perm(own, rcv, sel_hi);
+          }
+          // P goes to its S buffer's first 32 columns (it does not depend on O).
+          tmem_st16x64_x16(blk_addr + sb * kSCols, pw);
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run, mx);
-        const bool rescale = m_run != -INFINITY && m_new > m_run;
-        const float alpha = rescale ? exp2f(m_run - m_new) : 1.f;
-        m_run = m_new;
-
-        // P = 2^(s - m) * 256 as hi / lo e4m3; this lane's 64 keys -> 16 words of each
-        uint32_t hiw[16], low[16];
-        float psum = 0.f;
-#pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          float pv[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float sv = s[4 * w + k];
-            pv[k] = (sv == -INFINITY) ? 0.f : exp2f(sv - m_new);
-            psum += pv[k];
-          }
-          split4(pv[0] * 256.f, pv[1] * 256.f, pv[2] * 256.f, pv[3] * 256.f, hiw[w], low[w]);
-        }
-        l_part = l_part * alpha + psum;
-
-        // hi lanes gather every hi word of the row, lo lanes every lo word
-        uint32_t pw[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t send = is_hi ? low[4 * c + k] : hiw[4 * c + k];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            pw[8 * c + k] = is_hi ? hiw[4 * c + k] : recv;
-            pw[8 * c + 4 + k] = is_hi ? recv : low[4 * c + k];
-          }
-
         // O may only be touched once the previous tile's PV has completed
         if (j > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(u - 1) & 1]), ((u - 1) >> 1) & 1, abort_flag))) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(u - 1) & 1]), ((u - 1) >> 1) & 1, abort_flag))) { alive = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
+          if (warp_active && __any_sync(0xffffffffu, rescale)) {
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t v[32];
-              tmem_ld32(lane_addr + kOCol + 32 * c, v);
-              tmem_ld_wait(v);
+            for (int c = 0; c < 4; ++c) {
+              uint32_t a0[32];
+              tmem_ld16x256_x8(blk_addr + kOCol + 64 * c, a0);
+              tmem_ld_wait(a0);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(lane_addr + kOCol + 32 * c, v);
+              for (int i = 0; i < 32; i += 2) {
+                const float2 r0 = fmul2(make_float2(__uint_as_float(a0[i]), __uint_as_float(a0[i + 1])), a2);
+                a0[i] = __float_as_uint(r0.x);
+                a0[i + 1] = __float_as_uint(r0.y);
+              }
+              tmem_st16x256_x8(blk_addr + kOCol + 64 * c, a0);
             }
           }
         }
-        tmem_st32(lane_addr + sb * kSCols, pw);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.p_full[sb]));
       }
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      // All QK of this piece are complete (s_full of its last tile was waited), so Q can be
+      // rewritten for the next piece while this piece's last PV runs.
+      if (alive && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+        if (itn.k < prm.num_chunks && xn.ntiles == 0) {
+          trivial_item(xn);
+          itn = next_running(cursor_next(prm, itn), xn);
+        }
+        if (itn.k < prm.num_chunks && !prepare_q(xn, a_next)) alive = false;
+      }
+      if (!alive || __any_sync(0xffffffffu, *abort_flag != 0)) break;
 
-      // ---- epilogue: o = v_descale * (O_hi + O_lo / 16) / (256 l), lse = m + log2 l ---------
+      // ---- epilogue: o = v_descale * (O_hi + O_lo / 16) / l, lse = m + log2 l -----------------
       const uint32_t ul = t + x.ntiles - 1;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[ul & 1]), (ul >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      const float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
-      const float oscale = l > 0.f ? vd / (256.f * l) : 0.f;
-      float* orow = row_valid ? p.o_part + (out_row(p, x, rloc) * p.num_segments + x.s) * kHeadDim : nullptr;
+      float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);   // sum of p_s over the row's visible keys
+      if (warp_active) {
+        const float oscale = l > 0.f ? vd / l : 0.f;
+        const float2 wh = make_float2(oscale, oscale);
+        const float2 wl = make_float2(oscale * 0.0625f, oscale * 0.0625f);
+        float* orow = row_valid ? p.o_part + (out_row(p, x, rloc) * p.num_segments + x.s) * kHeadDim : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + kOCol + 32 * c, v);
-        tmem_ld_wait(v);
-        float o[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a0[32];
+          tmem_ld16x256_x8(blk_addr + kOCol + 64 * c, a0);
+          tmem_ld_wait(a0);
+          if (row_valid) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float mine = __uint_as_float(is_hi ? v[i] : v[16 + i]);
-          const float send = __uint_as_float(is_hi ? v[16 + i] : v[i]);
-          const float other = __shfl_xor_sync(0xffffffffu, send, 16);
-          o[i] = (is_hi ? fmaf(other, 0.0625f, mine) : fmaf(mine, 0.0625f, other)) * oscale;
+            for (int jj = 0; jj < 8; ++jj) {
+              const float2 h = make_float2(__uint_as_float(a0[4 * jj]), __uint_as_float(a0[4 * jj + 1]));
+              const float2 lo = make_float2(__uint_as_float(a0[4 * jj + 2]), __uint_as_float(a0[4 * jj + 3]));
+              const float2 o = ffma2(lo, wl, fmul2(h, wh));
+              *reinterpret_cast<float2*>(orow + 64 * c + 8 * jj + 2 * c4) = o;
+            }
+          }
         }
-        if (row_valid) {
-          float* dst = orow + 32 * c + (is_hi ? 0 : 16);
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
-        }
+        if (c4 == 0 && row_valid)
+          p.lse_part[out_row(p, x, rloc) * p.num_segments + x.s] =
+              l > 0.f ? m_ref + log2f(l) - kPShift : -INFINITY;
       }
-      if (is_hi && row_valid)
-        p.lse_part[out_row(p, x, rloc) * p.num_segments + x.s] = l > 0.f ? m_run + log2f(l) : -INFINITY;
+      close_unit(x);
       tc_fence_before();
       t += x.ntiles;
+      x = xn;
+      it = itn;
+      a_exp = a_next;
     }
   }
 
@@ -544,9 +715,18 @@ cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
   if (!make_cache_map(&prm.tmap_k, p.k_cache, p.num_pages, p.num_kv_heads) ||
       !make_cache_map(&prm.tmap_v, p.v_cache, p.num_pages, p.num_kv_heads))
     return cudaErrorInvalidValue;
-  const int64_t items = static_cast<int64_t>(p.num_segments) * p.num_seqs * p.num_kv_heads;
-  if (items > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  prm.num_items = static_cast<int32_t>(items);
+  const int sms0 = device_sm_count(-1);
+  if (sms0 <= 0) return cudaErrorInvalidDevice;
+  const int64_t V = p.max_pages;
+  const int64_t total = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * V;
+  int64_t C = V;
+  if (p.num_segments > 1) {
+    C = (total + sms0 - 1) / sms0;
+    const int64_t c_min = (V + p.num_segments - 2) / (p.num_segments - 1);
+    if (C < c_min) C = c_min;
+  }
+  prm.chunk_pages = C;
+  prm.num_chunks = (total + C - 1) / C;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static bool attr_set[64] = {false};
@@ -556,9 +736,7 @@ cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int sms = device_sm_count(-1);
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = static_cast<int>(items < sms ? items : sms);
+  const int grid = static_cast<int>(prm.num_chunks < sms0 ? prm.num_chunks : sms0);
   attn_main_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(prm);
   return cudaGetLastError();
 }

@@ -54,11 +54,13 @@ extern "C" int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv
   if (num_seqs <= 0 || num_kv_heads <= 0 || max_pages_per_seq <= 0) return MTPATTN_E_ARG;
   const int sms = device_sm_count(device);
   if (sms <= 0) return MTPATTN_E_DEVICE;
-  const long long units = static_cast<long long>(num_seqs) * num_kv_heads;
-  long long s = sms / units;
-  if (s < 1) s = 1;
+  // Enough split slots for a unit of max_pages_per_seq pages to be cut at every
+  // boundary of an equal per-SM share of the batch's pages.
+  const long long V = max_pages_per_seq;
+  const long long total = static_cast<long long>(num_seqs) * num_kv_heads * V;
+  const long long share = (total + sms - 1) / sms;
+  long long s = (V + share - 1) / share + 1;
   if (s > MTPATTN_MAX_SEGMENTS) s = MTPATTN_MAX_SEGMENTS;
-  if (s > max_pages_per_seq) s = max_pages_per_seq;
   return static_cast<int32_t>(s);
 }
 

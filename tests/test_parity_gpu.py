@@ -201,10 +201,14 @@ def test_host_pointers_are_refused():
 
 def test_num_segments_heuristic_on_device():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    s = api.mtp_verify_attn_num_segments(16, 1, 2188)
-    assert 1 <= s <= 64 and s * 16 <= max(sms, 16)
-    assert api.mtp_verify_attn_num_segments(1, 1, 3) == 3
-    assert api.mtp_verify_attn_num_segments(1000, 8, 100) == 1
+
+    def expect(b, hkv, v):
+        share = -(-(b * hkv * v) // sms)
+        return min(64, -(-v // share) + 1)
+
+    for args in ((16, 1, 2188), (1, 1, 3), (1000, 8, 100), (4, 1, 2188), (8, 1, 6563)):
+        s = api.mtp_verify_attn_num_segments(*args)
+        assert 1 <= s <= 64 and s == expect(*args), (args, s)
 
 
 @pytest.mark.parametrize("name,S", [("verify_16x35k_gqa16", 16), ("verify_16x35k_gqa8", 16),
