@@ -50,6 +50,9 @@
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+
 namespace mtpattn {
 namespace {
 
@@ -84,8 +87,9 @@ struct TcParams {
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   AttnParams a;
+  int64_t unit_pages;    // W >= max_pages: virtual pages per unit
   int64_t chunk_pages;   // C
-  int64_t num_chunks;    // ceil(units * max_pages / C)
+  int64_t num_chunks;    // ceil(units * W / C)
 };
 
 struct Bars {
@@ -106,11 +110,11 @@ struct Cursor {
 __device__ __forceinline__ Cursor cursor_first(const TcParams& prm) {
   Cursor c;
   c.k = blockIdx.x;
-  c.u = c.k * prm.chunk_pages / prm.a.max_pages;
+  c.u = c.k * prm.chunk_pages / prm.unit_pages;
   return c;
 }
 __device__ __forceinline__ Cursor cursor_next(const TcParams& prm, Cursor c) {
-  const int64_t V = prm.a.max_pages;
+  const int64_t V = prm.unit_pages;
   const int64_t end = min((c.k + 1) * prm.chunk_pages,
                           static_cast<int64_t>(prm.a.num_seqs) * prm.a.num_kv_heads * V);
   ++c.u;
@@ -130,7 +134,7 @@ struct Item {
 __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, int lane) {
   const AttnParams& p = prm.a;
   Item x;
-  const int64_t V = p.max_pages, C = prm.chunk_pages;
+  const int64_t V = prm.unit_pages, C = prm.chunk_pages;
   const int64_t k_first = c.u * V / C;
   x.s = static_cast<int>(c.k - k_first);
   x.last = c.k == (c.u * V + V - 1) / C;
@@ -155,17 +159,24 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
     x.pe = static_cast<int>(min(vp1, static_cast<int64_t>(n_pages)));
     if (x.pe < x.pb) x.pe = x.pb;
   }
-  if (!x.err && x.pe > x.pb) {
+  x.ntiles = x.err ? 0 : (x.pe - x.pb + kPagesPerTile - 1) / kPagesPerTile;
+  return x;
+}
+
+// Whether any block-table entry of the piece lies outside the page pool.  Only the
+// softmax warps check (while their Q loads are in flight); the producers load such a
+// page anyway -- a TMA box outside the tensor reads zeros -- and the piece's result is
+// then replaced by the error marker.
+__device__ __forceinline__ bool pages_bad(const AttnParams& p, const Item& x, int lane) {
+  int bad = 0;
+  if (x.pe > x.pb) {
     const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
-    int bad = 0;
     for (int i = x.pb + lane; i < x.pe; i += 32) {
       const int32_t e = bt[i];
       bad |= (e < 0 || e >= p.num_pages);
     }
-    if (__any_sync(0xffffffffu, bad)) x.err |= MTPATTN_ERR_PAGE;
   }
-  x.ntiles = x.err ? 0 : (x.pe - x.pb + kPagesPerTile - 1) / kPagesPerTile;
-  return x;
+  return __any_sync(0xffffffffu, bad) != 0;
 }
 
 __device__ __forceinline__ int64_t out_row(const AttnParams& p, const Item& x, int r) {
@@ -262,13 +273,19 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     fence_mbar_init();
   }
   // The V ring must hold finite values before any P = 0 column meets it.
-  for (int i = tid; i < (2 * kStages * kTileBytes) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(base + kOffK)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (kStages * kTileBytes) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(base + kOffV)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  // Launched as a programmatic dependent of the previous work on the stream: the set-up
+  // above touched no global memory; from here on inputs are read and the workspace is
+  // written, so wait until that work has completed and its results are visible.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // The segment reduce may be scheduled now; it waits for this grid's results itself.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   if (warp == 0 || warp == 10) {
     // ================================ producers (K: warp 0, V: warp 10) ============================
@@ -288,6 +305,10 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           const int pg0 = x.pb + j * kPagesPerTile;
           const int np = min(kPagesPerTile, x.pe - pg0);
           const int st = t % kStages;
+          // Start-up: the first K tile (and Q) go out alone, so they are not queued behind
+          // every SM's full rings; the rest follows once it has landed.
+          if ((t == 1 && !is_v) || (t == 0 && is_v))
+            if (!mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag)) break;
           if (!mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag)) break;
           const uint32_t fb = smem_u32(&full[st]);
           mbar_arrive_expect_tx(fb, np * 2 * 2048);
@@ -429,7 +450,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       xpar ^= 1;
       return ok;
     };
-    auto prepare_q = [&](const Item& y, int& a_exp_row) -> bool {
+    auto prepare_q = [&](const Item& y, int& a_exp_row, bool& bad_pages) -> bool {
       int a_exp = 0;
       const bool valid = q_row < y.R;
       uint4 w[16];                               // all 16 loads in flight at once
@@ -441,6 +462,9 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
                                    half * 128;
 #pragma unroll
         for (int c = 0; c < 16; ++c) w[c] = *reinterpret_cast<const uint4*>(src + 8 * c);
+      }
+      bad_pages = pages_bad(p, y, lane);        // its loads overlap the Q loads above
+      if (valid) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
@@ -488,7 +512,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     Item x;
     Cursor it = next_running(cursor_first(prm), x);
     int a_exp = 0;
-    bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp);
+    bool bad = false;
+    bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp, bad);
     while (alive && it.k < prm.num_chunks) {
       const bool row_valid = rloc < x.R;
       const bool warp_active = __any_sync(0xffffffffu, row_valid);
@@ -504,6 +529,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       itn.k = prm.num_chunks;
       itn.u = 0;
       int a_next = 0;
+      bool bad_next = false;
 
       for (int j = 0; j < x.ntiles; ++j) {
         const uint32_t u = t + j;
@@ -618,7 +644,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           trivial_item(xn);
           itn = next_running(cursor_next(prm, itn), xn);
         }
-        if (itn.k < prm.num_chunks && !prepare_q(xn, a_next)) alive = false;
+        if (itn.k < prm.num_chunks && !prepare_q(xn, a_next, bad_next)) alive = false;
       }
       if (!alive || __any_sync(0xffffffffu, *abort_flag != 0)) break;
 
@@ -650,7 +676,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         }
         if (c4 == 0 && row_valid)
           p.lse_part[out_row(p, x, rloc) * p.num_segments + x.s] =
-              l > 0.f ? m_ref + log2f(l) - kPShift : -INFINITY;
+              bad ? __int_as_float(0x7fc00000) : (l > 0.f ? m_ref + log2f(l) - kPShift : -INFINITY);
+        if (bad && lane == 0) set_status(p.status, MTPATTN_ERR_PAGE);
       }
       close_unit(x);
       tc_fence_before();
@@ -658,6 +685,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       x = xn;
       it = itn;
       a_exp = a_next;
+      bad = bad_next;
     }
   }
 
@@ -706,29 +734,81 @@ bool make_cache_map(CUtensorMap* map, const void* cache, int64_t num_pages, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoding a tensor map costs a few microseconds of host time: keep the last few.
+struct MapCacheEntry {
+  const void* k;
+  const void* v;
+  int64_t num_pages;
+  int hkv;
+  int device;
+  CUtensorMap mk, mv;
+};
+std::mutex g_map_mutex;
+MapCacheEntry g_map_cache[8];
+int g_map_next = 0;
+
+bool cache_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* mv) {
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  for (const MapCacheEntry& e : g_map_cache) {
+    if (e.k == p.k_cache && e.v == p.v_cache && e.num_pages == p.num_pages &&
+        e.hkv == p.num_kv_heads && e.device == device && e.k) {
+      *mk = e.mk;
+      *mv = e.mv;
+      return true;
+    }
+  }
+  MapCacheEntry& e = g_map_cache[g_map_next];
+  if (!make_cache_map(&e.mk, p.k_cache, p.num_pages, p.num_kv_heads) ||
+      !make_cache_map(&e.mv, p.v_cache, p.num_pages, p.num_kv_heads)) {
+    e.k = nullptr;
+    return false;
+  }
+  e.k = p.k_cache;
+  e.v = p.v_cache;
+  e.num_pages = p.num_pages;
+  e.hkv = p.num_kv_heads;
+  e.device = device;
+  g_map_next = (g_map_next + 1) % 8;
+  *mk = e.mk;
+  *mv = e.mv;
+  return true;
+}
+
 }  // namespace
 
 cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
   TcParams prm;
   prm.a = p;
   if (p.num_pages > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  if (!make_cache_map(&prm.tmap_k, p.k_cache, p.num_pages, p.num_kv_heads) ||
-      !make_cache_map(&prm.tmap_v, p.v_cache, p.num_pages, p.num_kv_heads))
-    return cudaErrorInvalidValue;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!cache_maps(p, dev, &prm.tmap_k, &prm.tmap_v)) return cudaErrorInvalidValue;
   const int sms0 = device_sm_count(-1);
   if (sms0 <= 0) return cudaErrorInvalidDevice;
   const int64_t V = p.max_pages;
-  const int64_t total = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * V;
-  int64_t C = V;
-  if (p.num_segments > 1) {
-    C = (total + sms0 - 1) / sms0;
-    const int64_t c_min = (V + p.num_segments - 2) / (p.num_segments - 1);
+  const int64_t U = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+  const int64_t S = p.num_segments;
+  // Equal shares of the whole virtual page line ...
+  int64_t W = V, C = V;
+  if (S > 1) {
+    C = (U * V + sms0 - 1) / sms0;
+    const int64_t c_min = (V + S - 2) / (S - 1);
     if (C < c_min) C = c_min;
+    // ... or, when every unit can get n >= 2 whole pieces for little extra per SM,
+    // cut each unit into exactly n pieces (unit stride n * C) so that no chunk holds
+    // two units (each extra piece costs a Q load and an epilogue on its SM).
+    const int64_t n = std::min<int64_t>(sms0 / U, S);
+    if (n >= 2) {
+      const int64_t c_al = (V + n - 1) / n;
+      if (c_al <= C + C / 8 + 16) {
+        C = c_al;
+        W = n * c_al;
+      }
+    }
   }
+  prm.unit_pages = W;
   prm.chunk_pages = C;
-  prm.num_chunks = (total + C - 1) / C;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  prm.num_chunks = (U * W + C - 1) / C;
   static bool attr_set[64] = {false};
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_main_tc_kernel,
@@ -737,7 +817,18 @@ cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   const int grid = static_cast<int>(prm.num_chunks < sms0 ? prm.num_chunks : sms0);
-  attn_main_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_main_tc_kernel, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -1,12 +1,16 @@
-// Split-KV segment reduce: merge the per-segment partial outputs of one query
-// row by their log-sum-exps and round to bf16 (the "split-KV segment reduce"
-// of the aiter PR #5190 page, Modifications).
+// Split-KV segment reduce: merge the per-slot partial outputs of one query row
+// by their log-sum-exps and round to bf16 (the split-KV segment reduce of the
+// aiter PR #5190 page, Modifications).
 //
 //   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s
 //
-// Segments with lse = -inf (empty, or no visible key) get weight 0 without
-// ever forming (-inf) - (-inf).  A NaN lse marks a row the main kernel flagged
-// as invalid; such rows are written as zeros.  One warp per row, 8 dims per lane.
+// Slots with lse = -inf (empty, or no visible key) get weight 0 and their
+// partial output is never used, so it need not have been written.  A NaN lse
+// marks a row the main kernel flagged as invalid; such rows are written as
+// zeros.  One warp per row, 8 dims per lane; the loads of 8 slots are in flight
+// together.  The kernel is launched as a programmatic dependent of the main
+// kernel: it may start while the main kernel drains and waits (griddepcontrol)
+// until the main kernel's results are visible.
 #include "common.cuh"
 
 #include <math.h>
@@ -14,10 +18,12 @@
 namespace mtpattn {
 namespace {
 
-constexpr int kWarpsPerCta = 8;
+constexpr int kWarpsPerCta = 4;
+constexpr int kGroup = 8;
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 attn_reduce_kernel(const AttnParams p) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
@@ -25,7 +31,7 @@ attn_reduce_kernel(const AttnParams p) {
   const int S = p.num_segments;
   const float* lse = p.lse_part + row * S;
 
-  // Each lane holds segments lane and lane + 32.
+  // Each lane holds slots lane and lane + 32.
   const float l0 = lane < S ? lse[lane] : -INFINITY;
   const float l1 = lane + 32 < S ? lse[lane + 32] : -INFINITY;
   int bad = isnan(l0) || isnan(l1);
@@ -41,16 +47,27 @@ attn_reduce_kernel(const AttnParams p) {
     const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
     const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
     const float* o = p.o_part + row * S * kHeadDim + lane * 8;
-    for (int s = 0; s < S; ++s) {
-      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      wsum += w;
-      if (w != 0.f) {
-        const float4 a = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim);
-        const float4 c = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim + 4);
-        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
-        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
-        acc[4] = fmaf(w, c.x, acc[4]); acc[5] = fmaf(w, c.y, acc[5]);
-        acc[6] = fmaf(w, c.z, acc[6]); acc[7] = fmaf(w, c.w, acc[7]);
+    for (int s0 = 0; s0 < S; s0 += kGroup) {
+      float4 a[kGroup], c[kGroup];
+      float w[kGroup];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int s = s0 + g;
+        w[g] = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+        if (s < S && w[g] != 0.f) {        // uniform across the warp (one row)
+          a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim);
+          c[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim + 4);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        if (s0 + g < S && w[g] != 0.f) {
+          wsum += w[g];
+          acc[0] = fmaf(w[g], a[g].x, acc[0]); acc[1] = fmaf(w[g], a[g].y, acc[1]);
+          acc[2] = fmaf(w[g], a[g].z, acc[2]); acc[3] = fmaf(w[g], a[g].w, acc[3]);
+          acc[4] = fmaf(w[g], c[g].x, acc[4]); acc[5] = fmaf(w[g], c[g].y, acc[5]);
+          acc[6] = fmaf(w[g], c[g].z, acc[6]); acc[7] = fmaf(w[g], c[g].w, acc[7]);
+        }
       }
     }
   }
@@ -70,8 +87,18 @@ attn_reduce_kernel(const AttnParams p) {
 
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  const unsigned grid = static_cast<unsigned>((rows + kWarpsPerCta - 1) / kWarpsPerCta);
-  attn_reduce_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kWarpsPerCta - 1) / kWarpsPerCta));
+  cfg.blockDim = dim3(kWarpsPerCta * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_reduce_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -56,7 +56,6 @@ __device__ inline void set_status(int32_t* status, int bits) {
 
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream);
-cudaError_t launch_attn_main_simt(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, int blocks,
                                cudaStream_t stream);
