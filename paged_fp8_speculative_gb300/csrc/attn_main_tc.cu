@@ -163,21 +163,6 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
   return x;
 }
 
-// Whether any block-table entry of the piece lies outside the page pool.  Only the
-// softmax warps check (while their Q loads are in flight); the producers load such a
-// page anyway -- a TMA box outside the tensor reads zeros -- and the piece's result is
-// then replaced by the error marker.
-__device__ __forceinline__ bool pages_bad(const AttnParams& p, const Item& x, int lane) {
-  int bad = 0;
-  if (x.pe > x.pb) {
-    const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
-    for (int i = x.pb + lane; i < x.pe; i += 32) {
-      const int32_t e = bt[i];
-      bad |= (e < 0 || e >= p.num_pages);
-    }
-  }
-  return __any_sync(0xffffffffu, bad) != 0;
-}
 
 __device__ __forceinline__ int64_t out_row(const AttnParams& p, const Item& x, int r) {
   const int t = r / p.ratio, g = r - t * p.ratio;
@@ -299,28 +284,33 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     uint32_t t = 0;  // global tile counter
     for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
-      if (lane == 0) {
-        const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
-        for (int j = 0; j < x.ntiles; ++j, ++t) {
-          const int pg0 = x.pb + j * kPagesPerTile;
-          const int np = min(kPagesPerTile, x.pe - pg0);
-          const int st = t % kStages;
+      const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
+      bool ok = true;
+      for (int j = 0; ok && j < x.ntiles; ++j, ++t) {
+        const int pg0 = x.pb + j * kPagesPerTile;
+        const int np = min(kPagesPerTile, x.pe - pg0);
+        const int st = t % kStages;
+        const int phys = lane < np ? bt[pg0 + lane] : 0;   // one page per lane, loads in parallel
+        const uint32_t fb = smem_u32(&full[st]);
+        if (lane == 0) {
           // Start-up: the first K tile (and Q) go out alone, so they are not queued behind
           // every SM's full rings; the rest follows once it has landed.
           if ((t == 1 && !is_v) || (t == 0 && is_v))
-            if (!mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag)) break;
-          if (!mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag)) break;
-          const uint32_t fb = smem_u32(&full[st]);
-          mbar_arrive_expect_tx(fb, np * 2 * 2048);
+            ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag);
+          ok = ok && mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(fb, np * 2 * 2048);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane < np) {
           const uint32_t dst = smem_u32(base + ring + st * kTileBytes);
-          for (int i = 0; i < np; ++i) {
-            const int phys = bt[pg0 + i];
-            tma_load_4d(dst + i * 2048, map, fb, 0, x.h, 0, phys, pol);
-            tma_load_4d(dst + kHalfBytes + i * 2048, map, fb, 128, x.h, 0, phys, pol);
-          }
+          tma_load_4d(dst + lane * 2048, map, fb, 0, x.h, 0, phys, pol);
+          tma_load_4d(dst + kHalfBytes + lane * 2048, map, fb, 128, x.h, 0, phys, pol);
         }
       }
-      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!ok) {
+        --t;                                   // the tile that failed was never issued
+        break;
+      }
     }
     // Never leave with copies in flight: wait for the last issued tiles of the ring.
     if (lane == 0) {
@@ -450,21 +440,22 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       xpar ^= 1;
       return ok;
     };
-    auto prepare_q = [&](const Item& y, int& a_exp_row, bool& bad_pages) -> bool {
+    // The hi and lo A rows of a query row (lanes l and l ^ 8 of the warp) need the same q
+    // values: the hi-row thread loads them and computes both code rows, and hands the lo
+    // codes to its partner.
+    auto prepare_q = [&](const Item& y, int& a_exp_row) -> bool {
       int a_exp = 0;
-      const bool valid = q_row < y.R;
+      const bool valid = q_row < y.R;            // same for both rows of the pair
+      const bool loader = valid && q_is_hi;
       uint4 w[16];                               // all 16 loads in flight at once
       float mx = 0.f;
-      if (valid) {
+      if (loader) {
         const int tk = q_row / p.ratio, g = q_row - tk * p.ratio;
         const __nv_bfloat16* src = p.q + static_cast<int64_t>(y.q0 + tk) * p.q_stride_tok +
                                    static_cast<int64_t>(y.h * p.ratio + g) * p.q_stride_head +
                                    half * 128;
 #pragma unroll
         for (int c = 0; c < 16; ++c) w[c] = *reinterpret_cast<const uint4*>(src + 8 * c);
-      }
-      bad_pages = pages_bad(p, y, lane);        // its loads overlap the Q loads above
-      if (valid) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
@@ -473,6 +464,10 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(ww[k] << 16)),
                                  fabsf(__uint_as_float(ww[k] & 0xFFFF0000u))));
         }
+      }
+      {
+        const float m_pair = __shfl_xor_sync(0xffffffffu, mx, 8);
+        if (!q_is_hi) mx = m_pair;
       }
       float mx_other;
       if (!exchange(mx, mx_other)) return false;
@@ -486,20 +481,22 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       unsigned char* qrow = base + kOffQ + half * (kQBytes / 2) + L32 * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {              // 8 output chunks of 16 codes
-        uint32_t out[4] = {0u, 0u, 0u, 0u};
-        if (valid) {
+        uint32_t hi4[4] = {0u, 0u, 0u, 0u}, lo4[4] = {0u, 0u, 0u, 0u};
+        if (loader) {
           const uint32_t ww[8] = {w[2 * c].x, w[2 * c].y, w[2 * c].z, w[2 * c].w,
                                   w[2 * c + 1].x, w[2 * c + 1].y, w[2 * c + 1].z, w[2 * c + 1].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t a0 = ww[2 * k], a1 = ww[2 * k + 1];
-            uint32_t hi, lo;
             split4(__uint_as_float(a0 << 16) * sc, __uint_as_float(a0 & 0xFFFF0000u) * sc,
-                   __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc, hi, lo);
-            out[k] = q_is_hi ? hi : lo;
+                   __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc,
+                   hi4[k], lo4[k]);
           }
         }
-        *reinterpret_cast<uint4*>(qrow + ((c ^ (L32 & 7)) * 16)) = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lo4[k] = __shfl_xor_sync(0xffffffffu, lo4[k], 8);
+        *reinterpret_cast<uint4*>(qrow + ((c ^ (L32 & 7)) * 16)) =
+            q_is_hi ? make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]) : make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.q_ready));
@@ -512,8 +509,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     Item x;
     Cursor it = next_running(cursor_first(prm), x);
     int a_exp = 0;
-    bool bad = false;
-    bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp, bad);
+    bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp);
     while (alive && it.k < prm.num_chunks) {
       const bool row_valid = rloc < x.R;
       const bool warp_active = __any_sync(0xffffffffu, row_valid);
@@ -529,11 +525,16 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       itn.k = prm.num_chunks;
       itn.u = 0;
       int a_next = 0;
-      bool bad_next = false;
+      // Whether a block-table entry of the piece lies outside the page pool: each tile's
+      // entries (read by the producers just before, so from L1) are checked during the tile.
+      bool bad = false;
+      const int32_t* bt_row = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
 
       for (int j = 0; j < x.ntiles; ++j) {
         const uint32_t u = t + j;
         const uint32_t sb = u & 1;
+        const int pg_lane = x.pb + j * kPagesPerTile + lane;
+        const int32_t bt_e = (lane < kPagesPerTile && pg_lane < x.pe) ? bt_row[pg_lane] : 0;
         if (j == x.ntiles - 1) {
           itn = cursor_next(prm, it);
           if (itn.k < prm.num_chunks) xn = item_info(prm, itn, lane);
@@ -636,6 +637,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.p_full[sb]));
+        bad |= __any_sync(0xffffffffu, bt_e < 0 || bt_e >= p.num_pages);
       }
       // All QK of this piece are complete (s_full of its last tile was waited), so Q can be
       // rewritten for the next piece while this piece's last PV runs.
@@ -644,7 +646,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           trivial_item(xn);
           itn = next_running(cursor_next(prm, itn), xn);
         }
-        if (itn.k < prm.num_chunks && !prepare_q(xn, a_next, bad_next)) alive = false;
+        if (itn.k < prm.num_chunks && !prepare_q(xn, a_next)) alive = false;
       }
       if (!alive || __any_sync(0xffffffffu, *abort_flag != 0)) break;
 
@@ -685,11 +687,11 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       x = xn;
       it = itn;
       a_exp = a_next;
-      bad = bad_next;
     }
   }
 
   // ---- teardown ------------------------------------------------------------------------------
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) set_status(p.status, MTPATTN_ERR_TIMEOUT);

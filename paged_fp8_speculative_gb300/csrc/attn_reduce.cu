@@ -24,6 +24,9 @@ constexpr int kGroup = 8;
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 attn_reduce_kernel(const AttnParams p) {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  // The next kernel on the stream (the next call's main kernel) may start its set-up now;
+  // it waits for this grid before it reads or writes anything this grid touches.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
