@@ -7,8 +7,8 @@
 // Slots with lse = -inf (empty, or no visible key) get weight 0 and their
 // partial output is never used, so it need not have been written.  A NaN lse
 // marks a row the main kernel flagged as invalid; such rows are written as
-// zeros.  One warp per row, 8 dims per lane; the loads of 8 slots are in flight
-// together.  The kernel is launched as a programmatic dependent of the main
+// zeros.  Two warps per row, 4 dims per lane; the loads of up to 16 slots are in
+// flight together.  The kernel is launched as a programmatic dependent of the main
 // kernel: it may start while the main kernel drains and waits (griddepcontrol)
 // until the main kernel's results are visible.
 #include "common.cuh"
@@ -19,7 +19,8 @@ namespace mtpattn {
 namespace {
 
 constexpr int kWarpsPerCta = 4;
-constexpr int kGroup = 8;
+constexpr int kWarpsPerRow = 2;     // each warp merges 128 of the row's 256 dims, 4 per lane
+constexpr int kGroup = 16;          // slots whose loads are in flight together
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 attn_reduce_kernel(const AttnParams p) {
@@ -28,7 +29,9 @@ attn_reduce_kernel(const AttnParams p) {
   // it waits for this grid before it reads or writes anything this grid touches.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t row = gw / kWarpsPerRow;
+  const int part = static_cast<int>(gw % kWarpsPerRow);
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
   if (row >= rows) return;
   const int S = p.num_segments;
@@ -44,46 +47,39 @@ attn_reduce_kernel(const AttnParams p) {
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     bad |= __shfl_xor_sync(0xffffffffu, bad, o);
   }
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (!bad && mx != -INFINITY) {
     const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
     const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
-    const float* o = p.o_part + row * S * kHeadDim + lane * 8;
+    const float* o = p.o_part + row * S * kHeadDim + part * 128 + lane * 4;
     for (int s0 = 0; s0 < S; s0 += kGroup) {
-      float4 a[kGroup], c[kGroup];
+      float4 a[kGroup];
       float w[kGroup];
 #pragma unroll
       for (int g = 0; g < kGroup; ++g) {
         const int s = s0 + g;
         w[g] = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-        if (s < S && w[g] != 0.f) {        // uniform across the warp (one row)
+        if (s < S && w[g] != 0.f)            // uniform across the warp (one row)
           a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim);
-          c[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim + 4);
-        }
       }
 #pragma unroll
       for (int g = 0; g < kGroup; ++g) {
         if (s0 + g < S && w[g] != 0.f) {
           wsum += w[g];
-          acc[0] = fmaf(w[g], a[g].x, acc[0]); acc[1] = fmaf(w[g], a[g].y, acc[1]);
-          acc[2] = fmaf(w[g], a[g].z, acc[2]); acc[3] = fmaf(w[g], a[g].w, acc[3]);
-          acc[4] = fmaf(w[g], c[g].x, acc[4]); acc[5] = fmaf(w[g], c[g].y, acc[5]);
-          acc[6] = fmaf(w[g], c[g].z, acc[6]); acc[7] = fmaf(w[g], c[g].w, acc[7]);
+          acc.x = fmaf(w[g], a[g].x, acc.x); acc.y = fmaf(w[g], a[g].y, acc.y);
+          acc.z = fmaf(w[g], a[g].z, acc.z); acc.w = fmaf(w[g], a[g].w, acc.w);
         }
       }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const int64_t tok = row / p.num_q_heads, head = row - tok * p.num_q_heads;
-  __nv_bfloat16* dst = p.out + tok * p.out_stride_tok + head * p.out_stride_head + lane * 8;
-  uint32_t packed[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-    packed[j] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  __nv_bfloat16* dst = p.out + tok * p.out_stride_tok + head * p.out_stride_head + part * 128 + lane * 4;
+  const __nv_bfloat162 v0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 v1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&v0),
+                                              *reinterpret_cast<const uint32_t*>(&v1));
 }
 
 }  // namespace
@@ -91,7 +87,7 @@ attn_reduce_kernel(const AttnParams p) {
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + kWarpsPerCta - 1) / kWarpsPerCta));
+  cfg.gridDim = dim3(static_cast<unsigned>((rows * kWarpsPerRow + kWarpsPerCta - 1) / kWarpsPerCta));
   cfg.blockDim = dim3(kWarpsPerCta * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
