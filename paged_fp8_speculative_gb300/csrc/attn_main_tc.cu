@@ -12,38 +12,41 @@
 // C = max_pages: one piece per unit.
 //
 // Roles (352 threads):
-//   warps 0, 10  producers of K (warp 0) and V (warp 10): TMA loads of the
-//              item's pages, straight from the paged NHD cache through the
-//              block table (two 128-byte-wide boxes per page, 128B-swizzled),
-//              into 3-stage K and V rings.  K and V run independently because
-//              a V slot frees one tile later than a K slot;
-//   warp 1     MMA issuer (one thread) and TMEM owner;
-//   warps 2-9  softmax: two groups of four warps.  Each group covers all 128
-//              TMEM lanes; group 0 owns key columns 0-63 of every tile (and O
-//              columns 0-127), group 1 key columns 64-127 (O columns 128-255).
+//   warp 0     K producer: per piece, first the piece's bf16 query rows (plain bulk copies
+//              into the Q buffer), then TMA loads of its K pages straight from the paged NHD
+//              cache through the block table (two 128-byte-wide boxes per page, 128B-swizzled)
+//              into a 3-stage ring;
+//   warp 10    V producer: the same for V (a V slot frees one tile later than a K slot);
+//   warp 1     MMA warp: runs warp-uniformly, one elected lane issues the tcgen05.mma
+//              instructions and their commits; it owns the TMEM allocation;
+//   warps 2-9  softmax: warp (quadrant q = w & 3, half g) owns TMEM lanes 32q + 16g .. +15.
 //
-// Precision.  Both contractions run as e4m3 x e4m3 -> f32 MMAs on the cache
-// bytes themselves, so K and V are never converted.  Q and P keep bf16-class
-// precision by writing each as the sum of two e4m3 terms:
+// Precision.  Both contractions run as e4m3 x e4m3 -> f32 MMAs on the cache bytes
+// themselves, so K and V are never converted.  Q and P keep bf16-class precision by writing
+// each as the sum of two e4m3 terms:
 //   Q:  x = q * 2^a (a per row, so max|x| is in [128, 256)),
-//       hi = e4m3(x), lo = e4m3((x - hi) * 16);  x = hi + lo/16 exactly for
-//       every element within 2^-13 of the row maximum (a bf16 value has 8
-//       significant bits: hi keeps 4 and the remainder fits lo's 4);
+//       hi = e4m3(x), lo = e4m3((x - hi) * 16);  x = hi + lo/16 exactly for every element
+//       within 2^-13 of the row maximum (a bf16 value has 8 significant bits: hi keeps 4
+//       and the remainder fits lo's 4);
 //   P:  p_s = 2^(s - m + 8 - kTau) in [0, 256] as hi + lo/16 the same way.
-// The hi and lo rows are stacked into one M = 128 MMA: TMEM lane 32w + t holds
-// hi (t < 16) or lo (t >= 16) of query row 16w + (t & 15), so the two halves
-// of a row sit in lanes t and t ^ 16 of one warp and are added with one
-// shuffle: S = hi + lo/16 per tile, O = O_hi + O_lo/16 at the end.
+// The hi and lo rows are stacked into one M = 128 MMA: query row r = 16q + 8g + a has its
+// hi row in TMEM lane 32q + 16g + a and its lo row 8 lanes below.  With the 16x256b access
+// shape one thread holds both lanes of its row, so S = hi + lo/16 is formed in registers,
+// and O = O_hi + O_lo/16 likewise in the epilogue.
 //
-// Online softmax with a lazy reference: m is only raised (and O rescaled in
-// TMEM) when a tile's row maximum exceeds it by more than kTau (log2 units);
-// otherwise p <= 2^kTau, which the P encoding scale 2^(8 - kTau) absorbs.
+// Online softmax with a lazy reference: m is only raised (and O rescaled in TMEM) when a
+// tile's row maximum exceeds it by more than kTau (log2 units); otherwise p <= 2^kTau,
+// which the P encoding scale 2^(8 - kTau) absorbs.
 //
-// Tile = 128 keys (8 pages).  TMEM: S double buffer at columns 0 and 128 (the
-// tile's P overwrites the first 32 columns of its S buffer, 4 e4m3 per column),
-// O at columns 256..511.  QK is 8 MMAs (K = 32 bytes each) with A = stacked Q
-// and B = the K tile (both K-major); PV is 4 MMAs with A = P from TMEM and
-// B = the V tile read MN-major (dims contiguous).
+// Tile = 128 keys (8 pages).  TMEM: S double buffer at columns 0 and 128 (the tile's P
+// overwrites the first 32 columns of its S buffer, 4 e4m3 per column), O at columns
+// 256..511.  QK is 8 MMAs (K = 32 bytes each) with A = stacked Q and B = the K tile (both
+// K-major); PV is 4 MMAs with A = P from TMEM and B = the V tile read MN-major.  The MMA
+// warp issues QK(u), PV(u-1), QK(u+1), ...: QK(u + 2) reuses the S buffer whose P(u) PV(u)
+// reads, and needs no wait for it because the MMAs of one thread execute in issue order.
+//
+// The kernel is launched as a programmatic dependent of the previous work on the stream and
+// lets the split-KV reduce be scheduled as soon as it starts.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -96,6 +99,8 @@ struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t q_ready, final_mma;
+  uint64_t q_land;                  // the piece's bf16 Q rows have landed in the Q buffer
+  uint64_t q_free;                  // the piece's last QK has completed: the Q buffer may be refilled
   uint64_t xbar[2];                 // cross-group exchange, one per slot parity
   uint32_t tmem_base;
   int32_t abort;
@@ -169,23 +174,32 @@ __device__ __forceinline__ int64_t out_row(const AttnParams& p, const Item& x, i
   return static_cast<int64_t>(x.q0 + t) * p.num_q_heads + x.h * p.ratio + g;
 }
 
-// Two floats -> two e4m3 codes (RN, saturating), first value in the low byte.
-__device__ __forceinline__ uint32_t f2_to_e4m3x2(float a, float b) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFF), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
 // Split x0..x3 into hi codes (4 bytes) and lo codes (4 bytes): x = hi + lo / 16.
+// hi = e4m3(x); the remainder x - hi is formed in f16 (exact: x rounded to f16 keeps 11
+// significant bits, hi 4, and their difference fits), scaled by 16 and rounded to e4m3.
 __device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, uint32_t& hi,
                                        uint32_t& lo) {
-  const uint32_t h01 = f2_to_e4m3x2(x0, x1), h23 = f2_to_e4m3x2(x2, x3);
-  const float2 g01 = e4m3x2_to_f2(h01), g23 = e4m3x2_to_f2(h23);
-  const uint32_t l01 = f2_to_e4m3x2((x0 - g01.x) * 16.f, (x1 - g01.y) * 16.f);
-  const uint32_t l23 = f2_to_e4m3x2((x2 - g23.x) * 16.f, (x3 - g23.y) * 16.f);
-  hi = h01 | (h23 << 16);
-  lo = l01 | (l23 << 16);
+  asm("{\n"
+      " .reg .b16 h01, h23, l01, l23;\n"
+      " .reg .b32 x01, x23, g01, g23, r01, r23, s16;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 h01, %3, %2;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 h23, %5, %4;\n"
+      " cvt.rn.f16x2.f32 x01, %3, %2;\n"
+      " cvt.rn.f16x2.f32 x23, %5, %4;\n"
+      " cvt.rn.f16x2.e4m3x2 g01, h01;\n"
+      " cvt.rn.f16x2.e4m3x2 g23, h23;\n"
+      " mov.b32 s16, 0x4C004C00;\n"
+      " sub.rn.f16x2 r01, x01, g01;\n"
+      " sub.rn.f16x2 r23, x23, g23;\n"
+      " mul.rn.f16x2 r01, r01, s16;\n"
+      " mul.rn.f16x2 r23, r23, s16;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 l01, r01;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 l23, r23;\n"
+      " mov.b32 %0, {h01, h23};\n"
+      " mov.b32 %1, {l01, l23};\n"
+      "}\n"
+      : "=r"(hi), "=r"(lo)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
 }
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
@@ -252,6 +266,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     }
     mbar_init(smem_u32(&bars.q_ready), kSoftmaxThreads);
     mbar_init(smem_u32(&bars.final_mma), 1);
+    mbar_init(smem_u32(&bars.q_land), 1);
+    mbar_init(smem_u32(&bars.q_free), 1);
     mbar_init(smem_u32(&bars.xbar[0]), kSoftmaxThreads);
     mbar_init(smem_u32(&bars.xbar[1]), kSoftmaxThreads);
     bars.abort = 0;
@@ -282,10 +298,44 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     if (lane == 0) prefetch_tmap(map);
     const uint64_t pol = l2_policy_evict_first();
     uint32_t t = 0;  // global tile counter
+    uint32_t n_q = 0;  // pieces whose Q rows this (K) producer has copied
+    bool q_failed = false;
     for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
       const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
       bool ok = true;
+      if (!is_v && x.ntiles > 0) {
+        // The piece's bf16 query rows go first (they are on the path to the first QK): row r
+        // (token r / ratio, head h * ratio + r % ratio) to byte r * 512 of the Q buffer, once
+        // the previous piece's last QK has stopped reading that buffer.
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&bars.q_free), (n_q & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(smem_u32(&bars.q_land), x.R * 2 * kHeadDim);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          q_failed = true;
+          break;
+        }
+        // Each copy instruction costs the TMA unit tens of cycles, so when the heads of a token
+        // are contiguous (the usual layout) one copy moves all `ratio` rows of a token.
+        if (p.q_stride_head == kHeadDim) {
+          if (lane < x.ql)
+            bulk_load(smem_u32(base + kOffQ + lane * p.ratio * 2 * kHeadDim),
+                      p.q + static_cast<int64_t>(x.q0 + lane) * p.q_stride_tok +
+                          static_cast<int64_t>(x.h) * p.ratio * kHeadDim,
+                      p.ratio * 2 * kHeadDim, smem_u32(&bars.q_land));
+        } else {
+          for (int r = lane; r < x.R; r += 32) {
+            const int tk = r / p.ratio, g = r - tk * p.ratio;
+            const __nv_bfloat16* src = p.q + static_cast<int64_t>(x.q0 + tk) * p.q_stride_tok +
+                                       static_cast<int64_t>(x.h * p.ratio + g) * p.q_stride_head;
+            bulk_load(smem_u32(base + kOffQ + r * 2 * kHeadDim), src, 2 * kHeadDim,
+                      smem_u32(&bars.q_land));
+          }
+        }
+        ++n_q;
+      }
       for (int j = 0; ok && j < x.ntiles; ++j, ++t) {
         const int pg0 = x.pb + j * kPagesPerTile;
         const int np = min(kPagesPerTile, x.pe - pg0);
@@ -312,7 +362,11 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         break;
       }
     }
-    // Never leave with copies in flight: wait for the last issued tiles of the ring.
+    // Never leave with copies in flight: wait for the last Q rows and the last issued tiles.
+    if (lane == 0 && n_q > 0 && !q_failed) {
+      volatile int no_abort = 0;
+      mbar_wait(smem_u32(&bars.q_land), (n_q - 1) & 1, &no_abort);
+    }
     if (lane == 0) {
       for (uint32_t k = 0; k < kStages && k < t; ++k) {
         const uint32_t u = t - 1 - k;
@@ -322,58 +376,73 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     }
   } else if (warp == 1) {
     // ======================================= MMA issuer =========================================
+    // The whole warp runs the loop, so every value it uses is warp-uniform; one elected lane
+    // issues the MMAs and their commits (a commit tracks the MMAs of the lane that issues it).
+    // The shared-memory descriptors are built once: operands move by whole 16-byte units,
+    // so advancing the 14-bit start-address field by (offset >> 4) never carries out of it.
     constexpr uint32_t kIdescQK = idesc_e4m3_f32(128, kTileKeys, false);
     constexpr uint32_t kIdescPV = idesc_e4m3_f32(128, kHeadDim, true);
-    const uint32_t q_addr = smem_u32(base + kOffQ);
+    const uint64_t q_desc = sdesc_sw128(smem_u32(base + kOffQ), 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(smem_u32(base + kOffK), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(base + kOffV), kHalfBytes, 1024);
+    const bool leader = elect_one();
     uint32_t t = 0;
     uint32_t items_run = 0;
+    auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort_flag));
+    };
+    auto issue_pv = [&](uint32_t u, bool first) -> bool {
+      const int st = u % kStages;
+      if (!wait_all(bars.v_full[st], (u / kStages) & 1)) return false;
+      if (!wait_all(bars.p_full[u & 1], (u >> 1) & 1)) return false;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t p_tmem = tmem + (u & 1) * kSCols;
+#pragma unroll
+        for (int k = 0; k < kTileKeys / 32; ++k)
+          mma_f8_ts(tmem + kOCol, p_tmem + 8 * k, v_desc + ((st * kTileBytes + k * 4096) >> 4),
+                    kIdescPV, (first && k == 0) ? 0u : 1u);
+        mma_commit(smem_u32(&bars.v_empty[st]));
+        mma_commit(smem_u32(&bars.pv_done[u & 1]));
+      }
+      __syncwarp();
+      return true;
+    };
     for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
       if (x.ntiles == 0) continue;
-      if (lane == 0) {
-        bool ok = mbar_wait(smem_u32(&bars.q_ready), items_run & 1, abort_flag);
+      bool ok = wait_all(bars.q_ready, items_run & 1);
+      tc_fence_after();
+      for (int j = 0; ok && j < x.ntiles; ++j) {
+        const uint32_t u = t + j;
+        const int st = u % kStages;
+        // S buffer u & 1 still holds P(u - 2) for PV(u - 2).  That PV was issued before this
+        // QK by this warp, and MMAs of one thread execute in issue order, so it reads P(u - 2)
+        // before QK(u) overwrites it: no wait on its completion is needed.
+        if (!wait_all(bars.k_full[st], (u / kStages) & 1)) { ok = false; break; }
         tc_fence_after();
-        auto issue_pv = [&](uint32_t u, bool first) -> bool {
-          const int st = u % kStages;
-          if (!mbar_wait(smem_u32(&bars.v_full[st]), (u / kStages) & 1, abort_flag)) return false;
-          if (!mbar_wait(smem_u32(&bars.p_full[u & 1]), (u >> 1) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(base + kOffV + st * kTileBytes);
-          const uint32_t p_tmem = tmem + (u & 1) * kSCols;
-#pragma unroll
-          for (int k = 0; k < kTileKeys / 32; ++k) {
-            const uint64_t bd = sdesc_sw128(v_addr + k * 4096, kHalfBytes, 1024);
-            mma_f8_ts(tmem + kOCol, p_tmem + 8 * k, bd, kIdescPV, (first && k == 0) ? 0u : 1u);
-          }
-          mma_commit(smem_u32(&bars.v_empty[st]));
-          mma_commit(smem_u32(&bars.pv_done[u & 1]));
-          return true;
-        };
-        for (int j = 0; ok && j < x.ntiles; ++j) {
-          const uint32_t u = t + j;
-          const int st = u % kStages;
-          if (!mbar_wait(smem_u32(&bars.k_full[st]), (u / kStages) & 1, abort_flag)) { ok = false; break; }
-          if (u >= 2 && !mbar_wait(smem_u32(&bars.pv_done[u & 1]), ((u - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(base + kOffK + st * kTileBytes);
+        if (leader) {
 #pragma unroll
           for (int k = 0; k < kHeadDim / 32; ++k) {
-            const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-            const uint64_t ad = sdesc_sw128(q_addr + (k >> 2) * (kQBytes / 2) + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k_addr + off, 16, 1024);
-            mma_f8_ss(tmem + (u & 1) * kSCols, ad, bd, kIdescQK, k > 0 ? 1u : 0u);
+            const uint32_t a_off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
+            const uint32_t b_off = st * kTileBytes + (k >> 2) * kHalfBytes + (k & 3) * 32;
+            mma_f8_ss(tmem + (u & 1) * kSCols, q_desc + (a_off >> 4), k_desc + (b_off >> 4),
+                      kIdescQK, k > 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&bars.s_full[u & 1]));
           mma_commit(smem_u32(&bars.k_empty[st]));
-          if (j > 0 && !issue_pv(u - 1, j == 1)) { ok = false; break; }
+          if (j == x.ntiles - 1) mma_commit(smem_u32(&bars.q_free));
         }
-        if (ok) issue_pv(t + x.ntiles - 1, x.ntiles == 1);
+        __syncwarp();
+        if (j > 0 && !issue_pv(u - 1, j == 1)) { ok = false; break; }
       }
+      if (ok) issue_pv(t + x.ntiles - 1, x.ntiles == 1);
       t += x.ntiles;
       ++items_run;
     }
-    if (lane == 0) {
-      mma_commit(smem_u32(&bars.final_mma));
+    if (leader) mma_commit(smem_u32(&bars.final_mma));
+    __syncwarp();
+    {
       volatile int no_abort = 0;
       mbar_wait(smem_u32(&bars.final_mma), 0, &no_abort);
     }
@@ -424,10 +493,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       }
       return c;
     };
-    // Q of piece y into the stacked A tile: this thread writes bytes half*128 .. +127 of
-    // A row L32.  The row's scale 2^a (max |q| * 2^a in [128, 256)) needs the max over
-    // both halves: the other half of row L32 is in warp (quad, half ^ 1), lane `lane`,
-    // exchanged through shared memory and the q_ready-independent xbar barriers.
+    // Value exchange with the same lane of warp (quad, half ^ 1) through shared memory and
+    // the xbar barriers (all 256 softmax threads arrive; the barrier alternates per call).
     int xpar = 0;
     uint32_t xphase = 0;
     auto exchange = [&](float v, float& other) -> bool {
@@ -440,35 +507,36 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       xpar ^= 1;
       return ok;
     };
-    // The hi and lo A rows of a query row (lanes l and l ^ 8 of the warp) need the same q
-    // values: the hi-row thread loads them and computes both code rows, and hands the lo
-    // codes to its partner.
+    // Q of piece y into the stacked A tile.  The producer has bulk-copied the piece's bf16
+    // rows into the Q buffer (row r at byte r * 512).  The pair of lanes l (hi A row of query
+    // row q_row) and l ^ 8 (its lo A row) shares that row's half `half`: each reads 64 of its
+    // 128 values and writes their hi codes to the hi A row and lo codes to the lo A row.  The
+    // row's scale 2^a (max |q| * 2^a in [128, 256)) needs the max over both halves, which
+    // sit in warp (quad, half ^ 1): the exchange gives it, and since every thread arrives
+    // only after its reads, it also frees the buffer for the codes that overwrite it.
+    uint32_t q_par = 0;
     auto prepare_q = [&](const Item& y, int& a_exp_row) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.q_land), q_par, abort_flag))) return false;
+      q_par ^= 1;
       int a_exp = 0;
-      const bool valid = q_row < y.R;            // same for both rows of the pair
-      const bool loader = valid && q_is_hi;
-      uint4 w[16];                               // all 16 loads in flight at once
+      const bool valid = q_row < y.R;
+      const int part = q_is_hi ? 0 : 1;
+      uint4 w[8];                                // chunk (i + lane) & 7: no bank conflicts
       float mx = 0.f;
-      if (loader) {
-        const int tk = q_row / p.ratio, g = q_row - tk * p.ratio;
-        const __nv_bfloat16* src = p.q + static_cast<int64_t>(y.q0 + tk) * p.q_stride_tok +
-                                   static_cast<int64_t>(y.h * p.ratio + g) * p.q_stride_head +
-                                   half * 128;
+      if (valid) {
+        const unsigned char* src = base + kOffQ + q_row * 2 * kHeadDim + half * kHeadDim + part * 128;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) w[c] = *reinterpret_cast<const uint4*>(src + 8 * c);
+        for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(src + ((i + lane) & 7) * 16);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t ww[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(ww[k] << 16)),
                                  fabsf(__uint_as_float(ww[k] & 0xFFFF0000u))));
         }
       }
-      {
-        const float m_pair = __shfl_xor_sync(0xffffffffu, mx, 8);
-        if (!q_is_hi) mx = m_pair;
-      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       float mx_other;
       if (!exchange(mx, mx_other)) return false;
       mx = fmaxf(mx, mx_other);
@@ -478,25 +546,24 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         a_exp = min(126, max(-126, 8 - e));      // mx * 2^a in [128, 256)
       }
       const float sc = pow2f(a_exp);
-      unsigned char* qrow = base + kOffQ + half * (kQBytes / 2) + L32 * 128;
+      const int l_hi = 32 * quad + (lane & ~8);
+      unsigned char* row_hi = base + kOffQ + half * (kQBytes / 2) + l_hi * 128;
+      unsigned char* row_lo = row_hi + 8 * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {              // 8 output chunks of 16 codes
-        uint32_t hi4[4] = {0u, 0u, 0u, 0u}, lo4[4] = {0u, 0u, 0u, 0u};
-        if (loader) {
-          const uint32_t ww[8] = {w[2 * c].x, w[2 * c].y, w[2 * c].z, w[2 * c].w,
-                                  w[2 * c + 1].x, w[2 * c + 1].y, w[2 * c + 1].z, w[2 * c + 1].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t a0 = ww[2 * k], a1 = ww[2 * k + 1];
-            split4(__uint_as_float(a0 << 16) * sc, __uint_as_float(a0 & 0xFFFF0000u) * sc,
-                   __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc,
-                   hi4[k], lo4[k]);
-          }
+      for (int i = 0; i < 8; ++i) {
+        const int c = (i + lane) & 7;            // source chunk: codes 8c .. 8c + 7 of this part
+        uint2 hi = make_uint2(0u, 0u), lo = make_uint2(0u, 0u);
+        if (valid) {
+          const uint32_t a0 = w[i].x, a1 = w[i].y, a2 = w[i].z, a3 = w[i].w;
+          split4(__uint_as_float(a0 << 16) * sc, __uint_as_float(a0 & 0xFFFF0000u) * sc,
+                 __uint_as_float(a1 << 16) * sc, __uint_as_float(a1 & 0xFFFF0000u) * sc, hi.x, lo.x);
+          split4(__uint_as_float(a2 << 16) * sc, __uint_as_float(a2 & 0xFFFF0000u) * sc,
+                 __uint_as_float(a3 << 16) * sc, __uint_as_float(a3 & 0xFFFF0000u) * sc, hi.y, lo.y);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) lo4[k] = __shfl_xor_sync(0xffffffffu, lo4[k], 8);
-        *reinterpret_cast<uint4*>(qrow + ((c ^ (L32 & 7)) * 16)) =
-            q_is_hi ? make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]) : make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+        const int byte = part * 64 + c * 8;      // within the 128-byte half row, before swizzling
+        const int off = (((byte >> 4) ^ (l_hi & 7)) << 4) + (byte & 15);
+        *reinterpret_cast<uint2*>(row_hi + off) = hi;
+        *reinterpret_cast<uint2*>(row_lo + off) = lo;
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.q_ready));
