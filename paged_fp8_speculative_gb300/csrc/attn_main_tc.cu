@@ -133,6 +133,7 @@ __device__ __forceinline__ Cursor cursor_next(const TcParams& prm, Cursor c) {
 // Geometry of one piece, computed identically by every role.
 struct Item {
   int s, b, h, L, q0, ql, R, pb, pe, ntiles, err;
+  int vp0;     // first virtual page of the piece (known before any load)
   bool last;   // the unit's last piece: it also marks the unit's unused slots empty
 };
 
@@ -147,6 +148,7 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
   x.h = static_cast<int>(c.u / p.num_seqs);
   const int64_t vp0 = max(c.k * C, c.u * V) - c.u * V;         // virtual page range of the piece
   const int64_t vp1 = min((c.k + 1) * C, (c.u + 1) * V) - c.u * V;
+  x.vp0 = static_cast<int>(vp0);
   x.L = p.seq_lens[x.b];
   x.q0 = p.cu_q[x.b];
   const int q1 = p.cu_q[x.b + 1];
@@ -304,21 +306,19 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       const Item x = item_info(prm, cur, lane);
       const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
       bool ok = true;
-      if (!is_v && x.ntiles > 0) {
-        // The piece's bf16 query rows go first (they are on the path to the first QK): row r
-        // (token r / ratio, head h * ratio + r % ratio) to byte r * 512 of the Q buffer, once
-        // the previous piece's last QK has stopped reading that buffer.
+      // Q rows of the piece (K producer only): row r (token r / ratio, head h * ratio +
+      // r % ratio) to byte r * 512 of the Q buffer, once the previous piece's last QK has
+      // stopped reading that buffer.  Each copy instruction costs the TMA unit tens of
+      // cycles, so when the heads of a token are contiguous (the usual layout) one copy
+      // moves all `ratio` rows of a token.
+      auto copy_q = [&]() -> bool {
+        bool q_ok = true;
         if (lane == 0) {
-          ok = mbar_wait(smem_u32(&bars.q_free), (n_q & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(smem_u32(&bars.q_land), x.R * 2 * kHeadDim);
+          q_ok = mbar_wait(smem_u32(&bars.q_free), (n_q & 1) ^ 1, abort_flag);
+          if (q_ok) mbar_arrive_expect_tx(smem_u32(&bars.q_land), x.R * 2 * kHeadDim);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          q_failed = true;
-          break;
-        }
-        // Each copy instruction costs the TMA unit tens of cycles, so when the heads of a token
-        // are contiguous (the usual layout) one copy moves all `ratio` rows of a token.
+        q_ok = __shfl_sync(0xffffffffu, q_ok, 0);
+        if (!q_ok) return false;
         if (p.q_stride_head == kHeadDim) {
           if (lane < x.ql)
             bulk_load(smem_u32(base + kOffQ + lane * p.ratio * 2 * kHeadDim),
@@ -335,16 +335,21 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           }
         }
         ++n_q;
-      }
+        return true;
+      };
       for (int j = 0; ok && j < x.ntiles; ++j, ++t) {
         const int pg0 = x.pb + j * kPagesPerTile;
         const int np = min(kPagesPerTile, x.pe - pg0);
         const int st = t % kStages;
-        const int phys = lane < np ? bt[pg0 + lane] : 0;   // one page per lane, loads in parallel
+        // One page per lane, loads in parallel.  The address comes from the cursor alone, so
+        // the first tile's entries are fetched together with the piece's lengths.
+        const int pg_spec = x.vp0 + j * kPagesPerTile + lane;
+        int phys = (lane < kPagesPerTile && pg_spec < p.max_pages) ? bt[pg_spec] : 0;
+        if (lane >= np) phys = 0;
         const uint32_t fb = smem_u32(&full[st]);
         if (lane == 0) {
-          // Start-up: the first K tile (and Q) go out alone, so they are not queued behind
-          // every SM's full rings; the rest follows once it has landed.
+          // Start-up: the first K tile goes out ahead of the other K tiles (and of every V
+          // tile), so that it is not queued behind them.
           if ((t == 1 && !is_v) || (t == 0 && is_v))
             ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag);
           ok = ok && mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag);
@@ -356,14 +361,21 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           tma_load_4d(dst + lane * 2048, map, fb, 0, x.h, 0, phys, pol);
           tma_load_4d(dst + kHalfBytes + lane * 2048, map, fb, 128, x.h, 0, phys, pol);
         }
+        // The piece's first K tile is on the way; its Q rows follow.
+        if (ok && j == 0 && !is_v && !copy_q()) {
+          q_failed = true;
+          ++t;                                   // the tile itself was issued
+          ok = false;
+          break;
+        }
       }
       if (!ok) {
-        --t;                                   // the tile that failed was never issued
+        if (!q_failed) --t;                    // the tile that failed was never issued
         break;
       }
     }
     // Never leave with copies in flight: wait for the last Q rows and the last issued tiles.
-    if (lane == 0 && n_q > 0 && !q_failed) {
+    if (lane == 0 && n_q > 0) {
       volatile int no_abort = 0;
       mbar_wait(smem_u32(&bars.q_land), (n_q - 1) & 1, &no_abort);
     }
@@ -472,7 +484,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     // reduce never reads the partial output of a slot whose weight is 0.
     auto close_unit = [&](const Item& y) {
       if (y.last && c4 == 0 && rloc < y.R)
-        for (int s2 = y.s + 1; s2 < p.num_segments; ++s2)
+        for (int s2 = y.s + 1; s2 < p.slots_used; ++s2)
           p.lse_part[out_row(p, y, rloc) * p.num_segments + s2] = -INFINITY;
     };
     // Pieces with nothing to compute: an error gets a NaN LSE (the reduce writes zeros),
@@ -845,7 +857,7 @@ bool cache_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* m
 
 }  // namespace
 
-cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream) {
   TcParams prm;
   prm.a = p;
   if (p.num_pages > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
@@ -878,6 +890,13 @@ cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream) {
   prm.unit_pages = W;
   prm.chunk_pages = C;
   prm.num_chunks = (U * W + C - 1) / C;
+  // A unit of W virtual pages touches at most ceil(W / C) + 1 chunks (exactly W / C when
+  // units are chunk-aligned): the reduce reads no slot beyond that.
+  {
+    const int64_t touch = (W % C == 0) ? W / C : (W + C - 1) / C + 1;
+    p.slots_used = static_cast<int32_t>(std::min<int64_t>(touch, p.num_segments));
+  }
+  prm.a = p;
   static bool attr_set[64] = {false};
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_main_tc_kernel,

@@ -5,7 +5,8 @@
 //   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s
 //
 // Slots with lse = -inf (empty, or no visible key) get weight 0 and their
-// partial output is never used, so it need not have been written.  A NaN lse
+// partial output is never used, so it need not have been written.  Only the
+// slots the main kernel's chunking can reach (slots_used) are read.  A NaN lse
 // marks a row the main kernel flagged as invalid; such rows are written as
 // zeros.  Two warps per row, 4 dims per lane; the loads of up to 16 slots are in
 // flight together.  The kernel is launched as a programmatic dependent of the main
@@ -35,40 +36,45 @@ attn_reduce_kernel(const AttnParams p) {
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
   if (row >= rows) return;
   const int S = p.num_segments;
+  const int n = p.slots_used;                // slots at or beyond n were never written
   const float* lse = p.lse_part + row * S;
+  const float* o = p.o_part + row * S * kHeadDim + part * 128 + lane * 4;
 
-  // Each lane holds slots lane and lane + 32.
-  const float l0 = lane < S ? lse[lane] : -INFINITY;
-  const float l1 = lane + 32 < S ? lse[lane + 32] : -INFINITY;
+  // Each lane holds slots lane and lane + 32.  The partial outputs of the first group are
+  // loaded together with the LSEs (one round trip); a slot whose weight turns out to be 0
+  // may hold anything, so its values are dropped by a select, never multiplied.
+  const float l0 = lane < n ? lse[lane] : -INFINITY;
+  const float l1 = lane + 32 < n ? lse[lane + 32] : -INFINITY;
+  float4 a[kGroup];
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g)
+    if (g < n) a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(g) * kHeadDim);
   int bad = isnan(l0) || isnan(l1);
   float mx = fmaxf(l0, l1);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  for (int off = 16; off > 0; off >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, off);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (!bad && mx != -INFINITY) {
     const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
     const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
-    const float* o = p.o_part + row * S * kHeadDim + part * 128 + lane * 4;
-    for (int s0 = 0; s0 < S; s0 += kGroup) {
-      float4 a[kGroup];
-      float w[kGroup];
+    for (int s0 = 0; s0 < n; s0 += kGroup) {
+      if (s0 > 0) {
 #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        const int s = s0 + g;
-        w[g] = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-        if (s < S && w[g] != 0.f)            // uniform across the warp (one row)
-          a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s) * kHeadDim);
+        for (int g = 0; g < kGroup; ++g)
+          if (s0 + g < n) a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + g) * kHeadDim);
       }
 #pragma unroll
       for (int g = 0; g < kGroup; ++g) {
-        if (s0 + g < S && w[g] != 0.f) {
-          wsum += w[g];
-          acc.x = fmaf(w[g], a[g].x, acc.x); acc.y = fmaf(w[g], a[g].y, acc.y);
-          acc.z = fmaf(w[g], a[g].z, acc.z); acc.w = fmaf(w[g], a[g].w, acc.w);
+        const int s2 = s0 + g;
+        const float w = __shfl_sync(0xffffffffu, s2 < 32 ? w0 : w1, s2 & 31);
+        if (s2 < n && w != 0.f) {                // uniform across the warp (one row)
+          wsum += w;
+          acc.x = fmaf(w, a[g].x, acc.x); acc.y = fmaf(w, a[g].y, acc.y);
+          acc.z = fmaf(w, a[g].z, acc.z); acc.w = fmaf(w, a[g].w, acc.w);
         }
       }
     }

@@ -31,6 +31,7 @@ struct AttnParams {
   const float* v_descale;
   float scale_log2;     // softmax_scale * log2(e): logits are kept in the log2 domain
   int32_t num_segments;
+  int32_t slots_used;    // slots the main kernel may write per row (<= num_segments); set by its launcher
   float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
   float* lse_part;      // [total_q * H_q][S] float32, log2-sum-exp2 of the segment (NaN = error)
   __nv_bfloat16* out;
@@ -55,7 +56,7 @@ __device__ inline void set_status(int32_t* status, int bits) {
 }
 
 // Host launchers (return cudaError_t of the launch).
-cudaError_t launch_attn_main(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, int blocks,
                                cudaStream_t stream);

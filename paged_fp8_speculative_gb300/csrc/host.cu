@@ -152,6 +152,7 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   p.v_descale = v_descale;
   p.scale_log2 = softmax_scale * kLog2e;
   p.num_segments = num_segments;
+  p.slots_used = num_segments;
   const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
   p.lse_part = static_cast<float*>(workspace);
   p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
