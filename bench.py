@@ -276,7 +276,7 @@ def run_ours(a) -> None:
                                                        batch.block_tables.shape[1])
     kd = torch.tensor([batch.k_descale], dtype=torch.float32, device=dev)
     vd = torch.tensor([batch.v_descale], dtype=torch.float32, device=dev)
-    ws = torch.empty(api.mtp_verify_attn_workspace_size(batch.total_q, batch.num_q_heads, S),
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(batch.total_q, batch.num_q_heads, S),
                      dtype=torch.uint8, device=dev)
     out = torch.empty_like(batch.q)
     stream = torch.cuda.current_stream()

@@ -26,6 +26,14 @@
  * does not use are written empty.  Any S in [1, 64] gives the same result up to
  * float32 re-association; S = 1 keeps every unit whole.
  *
+ * Balanced scheduling (the default): when every unit is cut into whole pieces
+ * and each SM holds one piece, the pieces of a unit share its 128-key tiles
+ * through a counter in the workspace, so SMs that stream faster take more
+ * tiles.  Which piece sums which tiles then varies from call to call: results
+ * agree to float32 re-association, not bit for bit.  After
+ * mtp_verify_attn_set_deterministic(1) every piece keeps a fixed page range and
+ * repeated calls are bit-identical.
+ *
  * Conventions for every entry point:
  *  - Pointers marked "device" must be CUDA device memory of the current device;
  *    the library never dereferences them on the host, never allocates, never
@@ -83,10 +91,11 @@ int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
                                      int32_t max_pages_per_seq, int32_t device);
 
 /*
- * Bytes of device workspace mtp_verify_attn_fwd needs:
- * float32 partial outputs [total_q * num_q_heads][num_segments][256] plus
- * float32 partial log-sum-exps [total_q * num_q_heads][num_segments], each
- * region 256-byte aligned.  Returns 0 for invalid arguments.
+ * Bytes of device workspace mtp_verify_attn_fwd needs: a 4096-byte header of
+ * tile counters (one per (sequence, KV head) unit, up to 1024 units), then
+ * float32 partial log-sum-exps [total_q * num_q_heads][num_segments], then
+ * float32 partial outputs [total_q * num_q_heads][num_segments][256], each region
+ * 256-byte aligned.  Returns 0 for invalid arguments.
  */
 size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int32_t num_segments);
 
@@ -106,9 +115,12 @@ size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int3
  *  v_descale
  *  softmax_scale  host float, multiplies the logits (usually 1/sqrt(256)).
  *  num_segments in [1, 64], or 0 for mtp_verify_attn_num_segments().
- *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned;
- *               its contents on entry do not matter; calls that overlap on the GPU
- *               must use different workspaces.
+ *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned.
+ *               Its first 4096 bytes (the counter header) must be zero before the
+ *               workspace's first use (e.g. one cudaMemset); every call, also one that
+ *               reports a device error, leaves them zero, so the workspace can be reused
+ *               by calls of any shape without clearing.  The rest need not be
+ *               initialised.  Calls that overlap on the GPU must use different workspaces.
  *  out          device bf16 [total_q][num_q_heads][256]; element strides out_stride_tok,
  *               out_stride_head (multiples of 8), unit stride along head_dim.
  *  status       optional device int32 (NULL = none); device-side MTPATTN_ERR_* bits are
@@ -149,10 +161,10 @@ int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_he
  * Calls needing more scratch than that (mtp_verify_attn_workspace_size() of the
  * resolved segment count) return MTPATTN_E_SCRATCH_LIMIT and launch nothing.
  * The first call on each device looks up the array's device address with that
- * device current and caches it; make that first call before any stream capture.
- * Every call on a device shares the one array and it keeps the last call's
- * contents, so calls that overlap on the GPU (other streams, other threads) race
- * on it and must be serialised by the caller.  Other return codes and the device
+ * device current, clears it (a synchronous cudaMemset) and caches the address; make
+ * that first call before any stream capture.
+ * Every call on a device shares the one array, so calls that overlap on the GPU
+ * (other streams, other threads) race on it and must be serialised by the caller.  Other return codes and the device
  * status bits are those of mtp_verify_attn_fwd.
  */
 int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
@@ -164,6 +176,14 @@ int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int6
                                        const float* v_descale, float softmax_scale,
                                        int32_t num_segments, void* out, int64_t out_stride_tok,
                                        int64_t out_stride_head, int32_t* status, void* stream);
+
+/*
+ * Process-wide scheduling switch for later calls: 1 = fixed page ranges per piece
+ * (bit-identical results across calls), 0 = balanced tile sharing (the default;
+ * see the top of this file).  Thread-safe; takes effect at the next launch.
+ */
+void mtp_verify_attn_set_deterministic(int32_t on);
+int32_t mtp_verify_attn_get_deterministic(void);
 
 /* Static description of a status code (never NULL). */
 const char* mtp_verify_attn_strerror(int status);

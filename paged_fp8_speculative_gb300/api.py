@@ -107,7 +107,7 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
         raise ValueError("out must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
     need = mtp_verify_attn_workspace_size(total_q, hq, num_segments)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     rc = lib().mtp_verify_attn_fwd(
         _ptr(q), q.stride(0), q.stride(1),
         _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -149,6 +149,15 @@ def mtp_verify_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor,
     if rc != OK:
         raise MtpAttnError(rc)
     return out
+
+
+def mtp_verify_attn_set_deterministic(on: bool) -> None:
+    """Fixed page ranges per piece (bit-identical repeats) instead of balanced tile sharing."""
+    lib().mtp_verify_attn_set_deterministic(1 if on else 0)
+
+
+def mtp_verify_attn_get_deterministic() -> bool:
+    return bool(lib().mtp_verify_attn_get_deterministic())
 
 
 def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, blocks: int = 0,

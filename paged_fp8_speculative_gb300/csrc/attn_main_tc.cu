@@ -81,7 +81,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kOffXchg = kOffBar + 256;                // 2 x 2 x 128 floats of cross-group exchange
+constexpr int kOffXchg = kOffBar + 512;                // 2 x 2 x 128 floats of cross-group exchange
 constexpr int kLayoutBytes = kOffXchg + 2 * 2 * 128 * 4;
 constexpr int kSmemBytes = 232448;
 static_assert(kLayoutBytes + 512 <= kSmemBytes, "shared-memory layout");
@@ -93,7 +93,11 @@ struct TcParams {
   int64_t unit_pages;    // W >= max_pages: virtual pages per unit
   int64_t chunk_pages;   // C
   int64_t num_chunks;    // ceil(units * W / C)
+  int32_t shared_tiles;  // 1: the pieces of a unit share its tiles (see the K producer)
+  int32_t pieces;        // pieces per unit when shared_tiles
 };
+
+constexpr int kRing = 16;              // entries of the tile-sequence ring
 
 struct Bars {
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
@@ -102,10 +106,12 @@ struct Bars {
   uint64_t q_land;                  // the piece's bf16 Q rows have landed in the Q buffer
   uint64_t q_free;                  // the piece's last QK has completed: the Q buffer may be refilled
   uint64_t xbar[2];                 // cross-group exchange, one per slot parity
+  uint64_t tid_full[kRing];         // ring entry e written (arrival count 1: the K producer)
+  int32_t tid[kRing];               // first page of the piece's next tile, or -1: piece done
   uint32_t tmem_base;
   int32_t abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Position in this CTA's walk: chunk k and unit u (unit = h * num_seqs + b).
 struct Cursor {
@@ -115,10 +121,20 @@ struct Cursor {
 __device__ __forceinline__ Cursor cursor_first(const TcParams& prm) {
   Cursor c;
   c.k = blockIdx.x;
-  c.u = c.k * prm.chunk_pages / prm.unit_pages;
+  // With shared tiles (one chunk per CTA) the pieces of a unit are CTAs u, u + U, u + 2U, ...
+  // rather than a run of neighbouring CTAs: neighbouring CTAs tend to land on the same part
+  // of the GPU, and parts of it stream at measurably different rates, so every unit gets a
+  // mix and the shared tiles even it out.
+  if (prm.shared_tiles) c.u = c.k % (static_cast<int64_t>(prm.a.num_seqs) * prm.a.num_kv_heads);
+  else c.u = c.k * prm.chunk_pages / prm.unit_pages;
   return c;
 }
 __device__ __forceinline__ Cursor cursor_next(const TcParams& prm, Cursor c) {
+  if (prm.shared_tiles) {                  // one unit per chunk
+    c.k += gridDim.x;
+    c.u = c.k % (static_cast<int64_t>(prm.a.num_seqs) * prm.a.num_kv_heads);
+    return c;
+  }
   const int64_t V = prm.unit_pages;
   const int64_t end = min((c.k + 1) * prm.chunk_pages,
                           static_cast<int64_t>(prm.a.num_seqs) * prm.a.num_kv_heads * V);
@@ -142,8 +158,13 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
   Item x;
   const int64_t V = prm.unit_pages, C = prm.chunk_pages;
   const int64_t k_first = c.u * V / C;
-  x.s = static_cast<int>(c.k - k_first);
-  x.last = c.k == (c.u * V + V - 1) / C;
+  if (prm.shared_tiles) {                  // slot = chunk / units; every slot of the unit runs
+    x.s = static_cast<int>(c.k / (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads));
+    x.last = false;
+  } else {
+    x.s = static_cast<int>(c.k - k_first);
+    x.last = c.k == (c.u * V + V - 1) / C;
+  }
   x.b = static_cast<int>(c.u % p.num_seqs);
   x.h = static_cast<int>(c.u / p.num_seqs);
   const int64_t vp0 = max(c.k * C, c.u * V) - c.u * V;         // virtual page range of the piece
@@ -165,6 +186,10 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
     x.pb = static_cast<int>(vp0);
     x.pe = static_cast<int>(min(vp1, static_cast<int64_t>(n_pages)));
     if (x.pe < x.pb) x.pe = x.pb;
+  }
+  if (prm.shared_tiles && !x.err) {        // the piece may take any tile of the unit
+    x.pb = 0;
+    x.pe = n_pages;
   }
   x.ntiles = x.err ? 0 : (x.pe - x.pb + kPagesPerTile - 1) / kPagesPerTile;
   return x;
@@ -272,6 +297,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     mbar_init(smem_u32(&bars.q_free), 1);
     mbar_init(smem_u32(&bars.xbar[0]), kSoftmaxThreads);
     mbar_init(smem_u32(&bars.xbar[1]), kSoftmaxThreads);
+    for (int i = 0; i < kRing; ++i) mbar_init(smem_u32(&bars.tid_full[i]), 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -299,13 +325,14 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     const int ring = is_v ? kOffV : kOffK;
     if (lane == 0) prefetch_tmap(map);
     const uint64_t pol = l2_policy_evict_first();
-    uint32_t t = 0;  // global tile counter
+    uint32_t t = 0;    // tiles issued by this producer
+    uint32_t e = 0;    // entries of the tile-sequence ring passed (tiles and end marks)
     uint32_t n_q = 0;  // pieces whose Q rows this (K) producer has copied
-    bool q_failed = false;
-    for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
+    bool stop = false;
+    for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !stop && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
+      if (x.ntiles == 0) continue;
       const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
-      bool ok = true;
       // Q rows of the piece (K producer only): row r (token r / ratio, head h * ratio +
       // r % ratio) to byte r * 512 of the Q buffer, once the previous piece's last QK has
       // stopped reading that buffer.  Each copy instruction costs the TMA unit tens of
@@ -337,41 +364,95 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         ++n_q;
         return true;
       };
-      for (int j = 0; ok && j < x.ntiles; ++j, ++t) {
-        const int pg0 = x.pb + j * kPagesPerTile;
+      // The piece's tile sequence is decided by the K producer and handed to every other
+      // role through the ring (first page of each tile, then -1).
+      //  - chunks: tiles 0 .. ntiles-1 of the piece (first page pb + 8 j);
+      //  - shared tiles (each CTA holds one piece, all pieces of a unit run together): piece s
+      //    of n takes tiles s and s + n of the unit, then tiles 2n + c with c claimed from the
+      //    unit's counter, so the unit's CTAs finish within about a tile of each other
+      //    whatever bandwidth each SM gets.  Claims run two tiles ahead of their use, and a
+      //    thread's successive claims increase, so a claim past the end is never followed by
+      //    a valid one it would drop.
+      uint32_t* ctr = p.tile_ctr + cur.u;
+      uint32_t c0 = 0, c1 = 0;                 // lane 0: claims in flight
+      for (int j = 0; ; ++j) {
+        int pg0 = -1;
+        if (!is_v) {
+          int idx = -1;
+          if (lane == 0) {
+            if (!prm.shared_tiles) {
+              idx = j < x.ntiles ? j : -1;
+            } else if (j < 2) {
+              idx = x.s + j * prm.pieces;
+              if (j == 0) c0 = atomicAdd(ctr, 1u); else c1 = atomicAdd(ctr, 1u);
+            } else {
+              idx = 2 * prm.pieces + static_cast<int>(c0);
+              c0 = c1;
+              if (idx < x.ntiles) c1 = atomicAdd(ctr, 1u);
+            }
+            if (idx >= x.ntiles) idx = -1;
+          }
+          idx = __shfl_sync(0xffffffffu, idx, 0);
+          pg0 = idx < 0 ? -1 : x.pb + idx * kPagesPerTile;
+        } else {
+          const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.tid_full[e % kRing]),
+                                                             (e / kRing) & 1, abort_flag));
+          if (!got) {
+            stop = true;
+            break;
+          }
+          pg0 = bars.tid[e % kRing];
+        }
+        if (pg0 < 0) {                         // end of the piece's sequence
+          if (!is_v && lane == 0) {
+            bars.tid[e % kRing] = -1;
+            mbar_arrive(smem_u32(&bars.tid_full[e % kRing]));
+          }
+          ++e;
+          if (j == 0 && !is_v && !copy_q()) stop = true;   // an empty piece still gets its Q
+          break;
+        }
         const int np = min(kPagesPerTile, x.pe - pg0);
         const int st = t % kStages;
-        // One page per lane, loads in parallel.  The address comes from the cursor alone, so
-        // the first tile's entries are fetched together with the piece's lengths.
-        const int pg_spec = x.vp0 + j * kPagesPerTile + lane;
+        // One page per lane, loads in parallel.  The first tile's address comes from the
+        // cursor alone, so its entries are fetched together with the piece's lengths.
+        const int pg_first = prm.shared_tiles ? x.s * kPagesPerTile : x.vp0;
+        const int pg_spec = (j == 0 ? pg_first : pg0) + lane;
         int phys = (lane < kPagesPerTile && pg_spec < p.max_pages) ? bt[pg_spec] : 0;
         if (lane >= np) phys = 0;
         const uint32_t fb = smem_u32(&full[st]);
+        bool ok = true;
         if (lane == 0) {
           // Start-up: the first K tile goes out ahead of the other K tiles (and of every V
           // tile), so that it is not queued behind them.
           if ((t == 1 && !is_v) || (t == 0 && is_v))
             ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag);
           ok = ok && mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(fb, np * 2 * 2048);
+          if (ok) {
+            if (!is_v) {                       // published once its K slot is free (ring bound)
+              bars.tid[e % kRing] = pg0;
+              mbar_arrive(smem_u32(&bars.tid_full[e % kRing]));
+            }
+            mbar_arrive_expect_tx(fb, np * 2 * 2048);
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok && lane < np) {
+        if (!ok) {
+          stop = true;
+          break;
+        }
+        if (lane < np) {
           const uint32_t dst = smem_u32(base + ring + st * kTileBytes);
           tma_load_4d(dst + lane * 2048, map, fb, 0, x.h, 0, phys, pol);
           tma_load_4d(dst + kHalfBytes + lane * 2048, map, fb, 128, x.h, 0, phys, pol);
         }
+        ++t;
+        ++e;
         // The piece's first K tile is on the way; its Q rows follow.
-        if (ok && j == 0 && !is_v && !copy_q()) {
-          q_failed = true;
-          ++t;                                   // the tile itself was issued
-          ok = false;
+        if (j == 0 && !is_v && !copy_q()) {
+          stop = true;
           break;
         }
-      }
-      if (!ok) {
-        if (!q_failed) --t;                    // the tile that failed was never issued
-        break;
       }
     }
     // Never leave with copies in flight: wait for the last Q rows and the last issued tiles.
@@ -420,13 +501,19 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       __syncwarp();
       return true;
     };
+    uint32_t e = 0;                            // tile-sequence ring entries passed
     for (Cursor cur = cursor_first(prm); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
       if (x.ntiles == 0) continue;
       bool ok = wait_all(bars.q_ready, items_run & 1);
       tc_fence_after();
-      for (int j = 0; ok && j < x.ntiles; ++j) {
-        const uint32_t u = t + j;
+      int j = 0;                               // tiles of this piece
+      while (ok) {
+        if (!wait_all(bars.tid_full[e % kRing], (e / kRing) & 1)) { ok = false; break; }
+        const int pg0 = bars.tid[e % kRing];
+        ++e;
+        if (pg0 < 0) break;
+        const uint32_t u = t;
         const int st = u % kStages;
         // S buffer u & 1 still holds P(u - 2) for PV(u - 2).  That PV was issued before this
         // QK by this warp, and MMAs of one thread execute in issue order, so it reads P(u - 2)
@@ -443,13 +530,17 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
           }
           mma_commit(smem_u32(&bars.s_full[u & 1]));
           mma_commit(smem_u32(&bars.k_empty[st]));
-          if (j == x.ntiles - 1) mma_commit(smem_u32(&bars.q_free));
         }
         __syncwarp();
         if (j > 0 && !issue_pv(u - 1, j == 1)) { ok = false; break; }
+        ++t;
+        ++j;
       }
-      if (ok) issue_pv(t + x.ntiles - 1, x.ntiles == 1);
-      t += x.ntiles;
+      if (!ok) break;
+      // Every QK of the piece is issued: the Q buffer is free once they complete.
+      if (leader) mma_commit(smem_u32(&bars.q_free));
+      __syncwarp();
+      if (j > 0 && !issue_pv(t - 1, j == 1)) break;
       ++items_run;
     }
     if (leader) mma_commit(smem_u32(&bars.final_mma));
@@ -584,7 +675,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       return true;
     };
 
-    uint32_t t = 0;
+    uint32_t t = 0;                            // tiles processed
+    uint32_t e = 0;                            // tile-sequence ring entries passed
     Item x;
     Cursor it = next_running(cursor_first(prm), x);
     int a_exp = 0;
@@ -599,7 +691,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       const float2 w_hi = make_float2(sscale, sscale);
       const float2 w_lo = make_float2(sscale * 0.0625f, sscale * 0.0625f);
       float m_ref = -INFINITY, l_part = 0.f;
-      Item xn;                                 // next piece, looked up during the last tile
+      Item xn;                                 // next piece
       Cursor itn;
       itn.k = prm.num_chunks;
       itn.u = 0;
@@ -609,15 +701,16 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       bool bad = false;
       const int32_t* bt_row = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
 
-      for (int j = 0; j < x.ntiles; ++j) {
+      int j = 0;                               // tiles of this piece
+      for (;; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.tid_full[e % kRing]), (e / kRing) & 1, abort_flag))) { alive = false; break; }
+        const int pg0 = bars.tid[e % kRing];   // first page of the tile, or -1: piece done
+        ++e;
+        if (pg0 < 0) break;
         const uint32_t u = t + j;
         const uint32_t sb = u & 1;
-        const int pg_lane = x.pb + j * kPagesPerTile + lane;
+        const int pg_lane = pg0 + lane;
         const int32_t bt_e = (lane < kPagesPerTile && pg_lane < x.pe) ? bt_row[pg_lane] : 0;
-        if (j == x.ntiles - 1) {
-          itn = cursor_next(prm, it);
-          if (itn.k < prm.num_chunks) xn = item_info(prm, itn, lane);
-        }
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[sb]), (u >> 1) & 1, abort_flag))) { alive = false; break; }
         tc_fence_after();
         float s[32];                           // s[2jj + e]: key 8jj + 2 c4 + e of the tile
@@ -641,7 +734,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
             s[2 * jj] = c0.x; s[2 * jj + 1] = c0.y;
             s[16 + 2 * jj] = c1.x; s[17 + 2 * jj] = c1.y;
           }
-          const int key0 = (x.pb + j * kPagesPerTile) * kPage + 2 * c4;
+          const int key0 = pg0 * kPage + 2 * c4;
           if (!__all_sync(0xffffffffu, key0 - 2 * c4 + kTileKeys - 1 <= vis_max)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -721,6 +814,8 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       // All QK of this piece are complete (s_full of its last tile was waited), so Q can be
       // rewritten for the next piece while this piece's last PV runs.
       if (alive && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+        itn = cursor_next(prm, it);
+        if (itn.k < prm.num_chunks) xn = item_info(prm, itn, lane);
         if (itn.k < prm.num_chunks && xn.ntiles == 0) {
           trivial_item(xn);
           itn = next_running(cursor_next(prm, itn), xn);
@@ -730,9 +825,12 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       if (!alive || __any_sync(0xffffffffu, *abort_flag != 0)) break;
 
       // ---- epilogue: o = v_descale * (O_hi + O_lo / 16) / l, lse = m + log2 l -----------------
-      const uint32_t ul = t + x.ntiles - 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[ul & 1]), (ul >> 1) & 1, abort_flag))) break;
-      tc_fence_after();
+      // (a piece may have taken no tile of its unit: then nothing was accumulated, lse = -inf)
+      if (j > 0) {
+        const uint32_t ul = t + j - 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[ul & 1]), (ul >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+      }
       float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);   // sum of p_s over the row's visible keys
       if (warp_active) {
@@ -741,7 +839,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
         const float2 wl = make_float2(oscale * 0.0625f, oscale * 0.0625f);
         float* orow = row_valid ? p.o_part + (out_row(p, x, rloc) * p.num_segments + x.s) * kHeadDim : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < (j > 0 ? 4 : 0); ++c) {
           uint32_t a0[32];
           tmem_ld16x256_x8(blk_addr + kOCol + 64 * c, a0);
           tmem_ld_wait(a0);
@@ -762,7 +860,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
       }
       close_unit(x);
       tc_fence_before();
-      t += x.ntiles;
+      t += j;
       x = xn;
       it = itn;
       a_exp = a_next;
@@ -890,6 +988,11 @@ cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream) {
   prm.unit_pages = W;
   prm.chunk_pages = C;
   prm.num_chunks = (U * W + C - 1) / C;
+  // When chunks never straddle units and every CTA holds one chunk, all pieces of a unit run
+  // at once and may share its tiles dynamically (per-unit counters in the workspace header).
+  prm.shared_tiles = (!p.deterministic && W % C == 0 && prm.num_chunks <= sms0 &&
+                      U <= kMaxTileCounters) ? 1 : 0;
+  prm.pieces = static_cast<int32_t>(W / C);
   // A unit of W virtual pages touches at most ceil(W / C) + 1 chunks (exactly W / C when
   // units are chunk-aligned): the reduce reads no slot beyond that.
   {

@@ -29,6 +29,11 @@ attn_reduce_kernel(const AttnParams p) {
   // The next kernel on the stream (the next call's main kernel) may start its set-up now;
   // it waits for this grid before it reads or writes anything this grid touches.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // The main kernel is complete: put its tile counters back to zero for the next call.
+  if (blockIdx.x == 0) {
+    const int units = min(p.num_seqs * p.num_kv_heads, kMaxTileCounters);
+    for (int i = threadIdx.x; i < units; i += blockDim.x) p.tile_ctr[i] = 0u;
+  }
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t row = gw / kWarpsPerRow;

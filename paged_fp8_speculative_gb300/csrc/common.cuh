@@ -32,6 +32,8 @@ struct AttnParams {
   float scale_log2;     // softmax_scale * log2(e): logits are kept in the log2 domain
   int32_t num_segments;
   int32_t slots_used;    // slots the main kernel may write per row (<= num_segments); set by its launcher
+  uint32_t* tile_ctr;    // per-unit tile counters (workspace header; zero between calls)
+  int32_t deterministic; // 1: fixed page ranges per piece (bit-identical repeats)
   float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
   float* lse_part;      // [total_q * H_q][S] float32, log2-sum-exp2 of the segment (NaN = error)
   __nv_bfloat16* out;
@@ -56,6 +58,11 @@ __device__ inline void set_status(int32_t* status, int bits) {
 }
 
 // Host launchers (return cudaError_t of the launch).
+// Workspace header: one tile counter per (sequence, KV head) unit, up to kMaxTileCounters
+// units (beyond that the pieces keep fixed page ranges).  Zero on entry, zero on return.
+constexpr int kMaxTileCounters = 1024;
+constexpr size_t kWorkspaceHeaderBytes = kMaxTileCounters * sizeof(uint32_t);
+
 cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, int blocks,

@@ -4,6 +4,7 @@
 #include "common.cuh"
 
 #include <math.h>
+#include <atomic>
 #include <stddef.h>
 
 namespace mtpattn {
@@ -26,6 +27,8 @@ int device_sm_count(int device) {
 }
 
 namespace {
+
+std::atomic<int> g_deterministic{0};   // scheduling switch, see mtp_verify_attn_set_deterministic
 
 constexpr size_t kAlign = 256;
 
@@ -72,7 +75,7 @@ extern "C" size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_
   const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
   const size_t lse = align_up(rows * num_segments * sizeof(float));
   const size_t o = align_up(rows * num_segments * kHeadDim * sizeof(float));
-  return lse + o;
+  return kWorkspaceHeaderBytes + lse + o;
 }
 
 extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
@@ -154,19 +157,24 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   p.num_segments = num_segments;
   p.slots_used = num_segments;
   const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
-  p.lse_part = static_cast<float*>(workspace);
-  p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+  p.tile_ctr = static_cast<uint32_t*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes);
+  p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes +
                                       align_up(rows * num_segments * sizeof(float)));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;
   p.status = status;
+  p.deterministic = g_deterministic.load(std::memory_order_relaxed);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_attn_main(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
   if (launch_attn_reduce(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
   return MTPATTN_OK;
 }
+
+extern "C" void mtp_verify_attn_set_deterministic(int32_t on) { g_deterministic.store(on ? 1 : 0); }
+extern "C" int32_t mtp_verify_attn_get_deterministic(void) { return g_deterministic.load(); }
 
 extern "C" const char* mtp_verify_attn_strerror(int status) {
   switch (status) {

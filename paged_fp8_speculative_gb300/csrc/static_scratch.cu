@@ -14,8 +14,9 @@
 // address, so the address the kernels get comes from cudaGetSymbolAddress,
 // looked up once per device with that device current (on the first call on
 // that device) and cached.  Every call shares the array: calls that overlap on
-// the GPU race on it.  The kernels write every partial they later read, so the
-// array needs no clearing between calls.
+// the GPU race on it.  The workspace's counter header must be zero when a call
+// starts: the array is cleared once, on the first call on its device, and every
+// call leaves the header zero again (the partials need no clearing).
 #include "common.cuh"
 
 #include <mutex>
@@ -34,7 +35,8 @@ void* scratch_address(int device) {
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_addr[device]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr ||
+        cudaMemset(ptr, 0, MTPATTN_STATIC_SCRATCH_BYTES) != cudaSuccess) {   // the entry state
       cudaGetLastError();
       return nullptr;
     }

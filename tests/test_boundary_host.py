@@ -44,8 +44,8 @@ def test_workspace_size():
     f = api.mtp_verify_attn_workspace_size
     rows = 64 * 16
     lse = (rows * 16 * 4 + 255) // 256 * 256
-    assert f(64, 16, 16) == lse + rows * 16 * 256 * 4
-    assert f(7, 8, 3) == ((7 * 8 * 3 * 4 + 255) // 256 * 256) + ((7 * 8 * 3 * 1024 + 255) // 256 * 256)
+    assert f(64, 16, 16) == 4096 + lse + rows * 16 * 256 * 4
+    assert f(7, 8, 3) == 4096 + ((7 * 8 * 3 * 4 + 255) // 256 * 256) + ((7 * 8 * 3 * 1024 + 255) // 256 * 256)
     assert f(64, 16, 0) == 0 and f(64, 16, 65) == 0 and f(-1, 16, 4) == 0 and f(4, 0, 4) == 0
 
 
@@ -126,3 +126,13 @@ def test_stream_read_argument_checks():
     assert f(None, 1024, FAKE, 4, None) == api.E_ARG
     assert f(FAKE, 1000, FAKE, 4, None) == api.E_ARG       # not a multiple of 16
     assert f(FAKE, 1024, None, 4, None) == api.E_ARG
+
+
+def test_deterministic_switch():
+    assert not api.mtp_verify_attn_get_deterministic()
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        assert api.mtp_verify_attn_get_deterministic()
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+    assert not api.mtp_verify_attn_get_deterministic()

@@ -133,11 +133,20 @@ def test_strided_q_and_out_views():
 
 
 def test_repeatable_and_graph_replay_bit_identical():
+    """Deterministic scheduling: repeated calls and a graph replay are bit-identical."""
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        _repeatable_and_graph_replay()
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
+def _repeatable_and_graph_replay():
     batch = synth.make_batch([5000, 2000], 4, 16, 1, seed=50).to("cuda")
     kd = torch.tensor([batch.k_descale], device="cuda")
     vd = torch.tensor([batch.v_descale], device="cuda")
     S = 8
-    ws = torch.empty(api.mtp_verify_attn_workspace_size(batch.total_q, 16, S), dtype=torch.uint8,
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(batch.total_q, 16, S), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty_like(batch.q)
     args = (batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
@@ -163,6 +172,41 @@ def test_repeatable_and_graph_replay_bit_identical():
     g.replay()
     torch.cuda.synchronize()
     assert not torch.equal(out, eager)
+
+
+def test_balanced_scheduling_repeats_within_reassociation():
+    """Balanced scheduling (the default) lets the pieces of a unit share its tiles: the
+    split differs from call to call, the result only by float32 re-association, and the
+    tile counters in the workspace header are back at zero after every call."""
+    assert not api.mtp_verify_attn_get_deterministic()
+    batch = synth.make_batch([5000, 5000], 4, 16, 1, seed=51, k_descale=0.5, v_descale=2.0)
+    ref = oracle.verify_attention(*oracle_args(batch))
+    gb = batch.to("cuda")
+    kd = torch.tensor([gb.k_descale], device="cuda")
+    vd = torch.tensor([gb.v_descale], device="cuda")
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(gb.total_q, 16, 16), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for _ in range(4):
+        o = api.mtp_verify_attn_fwd(gb.q, gb.k_cache, gb.v_cache, gb.block_tables, gb.seq_lens,
+                                    gb.cu_seqlens_q, kd, vd, gb.softmax_scale, num_segments=16,
+                                    workspace=ws)
+        torch.cuda.synchronize()
+        assert ws[:4096].count_nonzero().item() == 0
+        outs.append(o.float().cpu().numpy().astype(np.float64))
+    for o in outs:
+        assert oracle.excess_over_half_ulp(o, ref) <= TOL
+    scale = np.abs(outs[0]).max()
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 2 ** -7 * scale
+
+
+def test_deterministic_mode_matches_oracle():
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        check(synth.make_batch([5000, 5000, 31], [4, 2, 1], 16, 1, seed=52), num_segments=16)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
 
 
 def test_device_errors_set_status_and_zero_rows():
