@@ -5,8 +5,8 @@ pool, launches issued during CUDA graph capture, loops that must never
 synchronise the device), so this entry point keeps its split-KV partials in a
 library-owned static device array.  The test calls it through the C ABI twice in
 a row, on different batches, and checks each output against the regular entry
-point (which uses a caller workspace) within the parity tolerance of the other
-GPU tests.  It also checks that a call too large for the array is refused.
+point (which uses a caller workspace): bit for bit, under deterministic
+scheduling.  It also checks that a call too large for the array is refused.
 This file is collected last so a stop-at-first-failure run has run every other
 test before it; it passes alone in a fresh process as well.
 """
@@ -42,6 +42,15 @@ def _regular(b, kd, vd, S):
 
 
 def test_static_scratch_matches_regular_entry_point_twice():
+    # Deterministic scheduling, so the two entry points must agree bit for bit.
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        _static_vs_regular()
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
+def _static_vs_regular():
     batches = [
         synth.make_batch([3000, 1000, 77], [4, 2, 1], 16, 1, seed=901, k_descale=0.5,
                          v_descale=2.0).to("cuda"),
@@ -61,6 +70,7 @@ def test_static_scratch_matches_regular_entry_point_twice():
         o = out.float().cpu().numpy().astype(np.float64)
         assert np.isfinite(o).all()
         assert np.abs(o - r).max() / r.std() <= TOL
+        assert np.array_equal(o, r)
 
 
 def test_static_scratch_refuses_calls_beyond_its_size():
