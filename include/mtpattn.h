@@ -185,6 +185,22 @@ int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int6
 void mtp_verify_attn_set_deterministic(int32_t on);
 int32_t mtp_verify_attn_get_deterministic(void);
 
+/*
+ * How the split-KV pieces are laid out over the SMs (process-wide switch):
+ *  - MTPATTN_SCHED_CHUNKED (the default): from the host-side shape alone, every
+ *    (sequence, KV head) unit is cut as if it held max_pages pages.  Best when the
+ *    batch's lengths are close to max_pages; short sequences leave their SMs idle.
+ *  - MTPATTN_SCHED_PLANNED (at most 256 units, no more units than SMs): the main
+ *    kernel reads seq_lens first and gives each unit a number of pieces in
+ *    proportion to its length, so ragged batches keep every SM streaming.
+ * Returns MTPATTN_E_ARG for an unknown mode.  Thread-safe; takes effect at the
+ * next launch.
+ */
+#define MTPATTN_SCHED_CHUNKED 0
+#define MTPATTN_SCHED_PLANNED 1
+int32_t mtp_verify_attn_set_scheduling(int32_t mode);
+int32_t mtp_verify_attn_get_scheduling(void);
+
 /* Static description of a status code (never NULL). */
 const char* mtp_verify_attn_strerror(int status);
 

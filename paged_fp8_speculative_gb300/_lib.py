@@ -35,6 +35,8 @@ SIGNATURES = {
         _vp, _c_i64, _c_i64, _vp, _vp]),
     "mtp_verify_attn_set_deterministic": (None, [_c_i32]),
     "mtp_verify_attn_get_deterministic": (_c_i32, []),
+    "mtp_verify_attn_set_scheduling": (_c_i32, [_c_i32]),
+    "mtp_verify_attn_get_scheduling": (_c_i32, []),
     "mtp_verify_attn_strerror": (ctypes.c_char_p, [_c_int]),
     "mtpattn_stream_read": (_c_int, [_vp, _c_size, _vp, _c_i32, _vp]),
     "mtpattn_stream_read_default_blocks": (_c_i32, []),

@@ -160,6 +160,21 @@ def mtp_verify_attn_get_deterministic() -> bool:
     return bool(lib().mtp_verify_attn_get_deterministic())
 
 
+SCHED_CHUNKED = 0
+SCHED_PLANNED = 1
+
+
+def mtp_verify_attn_set_scheduling(mode: int) -> None:
+    """Chunked (0, sized for max_pages) or planned (1, sized from seq_lens on the device)."""
+    rc = lib().mtp_verify_attn_set_scheduling(int(mode))
+    if rc != OK:
+        raise ValueError(f"unknown scheduling mode {mode}")
+
+
+def mtp_verify_attn_get_scheduling() -> int:
+    return int(lib().mtp_verify_attn_get_scheduling())
+
+
 def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, blocks: int = 0,
                         stream=None) -> torch.Tensor:
     """Read every byte of ``buf`` once (streaming-read ceiling probe); returns the sink."""

@@ -160,7 +160,7 @@ __device__ __forceinline__ Item item_info(const TcParams& prm, const Cursor& c, 
   const int64_t k_first = c.u * V / C;
   if (prm.shared_tiles) {                  // slot = chunk / units; every slot of the unit runs
     x.s = static_cast<int>(c.k / (static_cast<int64_t>(p.num_seqs) * p.num_kv_heads));
-    x.last = false;
+    x.last = x.s == prm.pieces - 1;        // it also marks the unit's unused slots empty
   } else {
     x.s = static_cast<int>(c.k - k_first);
     x.last = c.k == (c.u * V + V - 1) / C;
@@ -575,7 +575,7 @@ attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
     // reduce never reads the partial output of a slot whose weight is 0.
     auto close_unit = [&](const Item& y) {
       if (y.last && c4 == 0 && rloc < y.R)
-        for (int s2 = y.s + 1; s2 < p.slots_used; ++s2)
+        for (int s2 = y.s + 1; s2 < p.num_segments; ++s2)
           p.lse_part[out_row(p, y, rloc) * p.num_segments + s2] = -INFINITY;
     };
     // Pieces with nothing to compute: an error gets a NaN LSE (the reduce writes zeros),
@@ -955,7 +955,16 @@ bool cache_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* m
 
 }  // namespace
 
+bool kv_tensor_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* mv) {
+  return cache_maps(p, device, mk, mv);
+}
+
 cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream) {
+  if (p.scheduling == MTPATTN_SCHED_PLANNED) {
+    const int sms = device_sm_count(-1);
+    const int64_t units = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+    if (sms > 0 && units <= kPlanUnits && units <= sms) return launch_attn_main_planned(p, stream);
+  }
   TcParams prm;
   prm.a = p;
   if (p.num_pages > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;

@@ -5,13 +5,18 @@
 //   M = max_s lse_s,  w_s = 2^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s
 //
 // Slots with lse = -inf (empty, or no visible key) get weight 0 and their
-// partial output is never used, so it need not have been written.  Only the
-// slots the main kernel's chunking can reach (slots_used) are read.  A NaN lse
+// partial output is never used, so it need not have been written.  A NaN lse
 // marks a row the main kernel flagged as invalid; such rows are written as
-// zeros.  Two warps per row, 4 dims per lane; the loads of up to 16 slots are in
-// flight together.  The kernel is launched as a programmatic dependent of the main
-// kernel: it may start while the main kernel drains and waits (griddepcontrol)
-// until the main kernel's results are visible.
+// zeros.  The kernel is launched as a programmatic dependent of the main kernel:
+// it may start while the main kernel drains and waits (griddepcontrol) until the
+// main kernel's results are visible.
+//
+// Work split: the S slots of a row form ceil(S / 16) groups of 16, and each
+// (group, half of the row's 256 dims) pair is one warp, 4 dims per lane.  Every
+// warp reads all S LSEs (two per lane: the same few cache lines), so each knows M
+// and the weight sum; its own group's partial outputs are in flight together, so
+// a row costs one round trip of loads whatever S is.  Groups other than the first
+// hand their weighted sums to the first through shared memory.
 #include "common.cuh"
 
 #include <math.h>
@@ -19,12 +24,14 @@
 namespace mtpattn {
 namespace {
 
-constexpr int kWarpsPerCta = 4;
-constexpr int kWarpsPerRow = 2;     // each warp merges 128 of the row's 256 dims, 4 per lane
-constexpr int kGroup = 16;          // slots whose loads are in flight together
+constexpr int kGroup = 16;          // slots per warp
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-attn_reduce_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(256)
+attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
+  // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic,
+  // and none at all for S <= 16, so that the reduce's CTAs fit beside a finishing main-kernel
+  // CTA that still holds nearly all of its SM's shared memory.
+  extern __shared__ float4 xfer[];
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   // The next kernel on the stream (the next call's main kernel) may start its set-up now;
   // it waits for this grid before it reads or writes anything this grid touches.
@@ -35,25 +42,27 @@ attn_reduce_kernel(const AttnParams p) {
     for (int i = threadIdx.x; i < units; i += blockDim.x) p.tile_ctr[i] = 0u;
   }
   const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
-  const int64_t row = gw / kWarpsPerRow;
-  const int part = static_cast<int>(gw % kWarpsPerRow);
+  const int warp = threadIdx.x >> 5;
+  const int wpr = 2 * groups;                      // warps per row
+  const int g = (warp % wpr) >> 1;                 // slot group of this warp
+  const int part = warp & 1;                       // half of the row's dims
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + warp / wpr;
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  if (row >= rows) return;
+  const bool live = row < rows;
   const int S = p.num_segments;
-  const int n = p.slots_used;                // slots at or beyond n were never written
-  const float* lse = p.lse_part + row * S;
-  const float* o = p.o_part + row * S * kHeadDim + part * 128 + lane * 4;
-
-  // Each lane holds slots lane and lane + 32.  The partial outputs of the first group are
-  // loaded together with the LSEs (one round trip); a slot whose weight turns out to be 0
-  // may hold anything, so its values are dropped by a select, never multiplied.
-  const float l0 = lane < n ? lse[lane] : -INFINITY;
-  const float l1 = lane + 32 < n ? lse[lane + 32] : -INFINITY;
+  const int s_lo = g * kGroup;
+  // Slots below slots_used are the ones most rows use: their partial outputs are loaded
+  // together with the LSEs.  Others of the group only where their weight is not 0.  A slot
+  // of weight 0 may hold anything, so its values are dropped by a select, never multiplied.
+  const int n_spec = live ? max(0, min(min(p.slots_used, S) - s_lo, kGroup)) : 0;
+  const float* lse = p.lse_part + (live ? row : 0) * S;
+  const float* o = p.o_part + ((live ? row : 0) * S + s_lo) * kHeadDim + part * 128 + lane * 4;
+  const float l0 = live && lane < S ? lse[lane] : -INFINITY;
+  const float l1 = live && lane + 32 < S ? lse[lane + 32] : -INFINITY;
   float4 a[kGroup];
 #pragma unroll
-  for (int g = 0; g < kGroup; ++g)
-    if (g < n) a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(g) * kHeadDim);
+  for (int i = 0; i < kGroup; ++i)
+    if (i < n_spec) a[i] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(i) * kHeadDim);
   int bad = isnan(l0) || isnan(l1);
   float mx = fmaxf(l0, l1);
 #pragma unroll
@@ -66,24 +75,35 @@ attn_reduce_kernel(const AttnParams p) {
   if (!bad && mx != -INFINITY) {
     const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
     const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
-    for (int s0 = 0; s0 < n; s0 += kGroup) {
-      if (s0 > 0) {
+    wsum = w0 + w1;
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g)
-          if (s0 + g < n) a[g] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + g) * kHeadDim);
-      }
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    float w[kGroup];
 #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        const int s2 = s0 + g;
-        const float w = __shfl_sync(0xffffffffu, s2 < 32 ? w0 : w1, s2 & 31);
-        if (s2 < n && w != 0.f) {                // uniform across the warp (one row)
-          wsum += w;
-          acc.x = fmaf(w, a[g].x, acc.x); acc.y = fmaf(w, a[g].y, acc.y);
-          acc.z = fmaf(w, a[g].z, acc.z); acc.w = fmaf(w, a[g].w, acc.w);
-        }
+    for (int i = 0; i < kGroup; ++i) {
+      const int s2 = s_lo + i;
+      w[i] = __shfl_sync(0xffffffffu, s2 < 32 ? w0 : w1, s2 & 31);   // 0 for s2 >= S
+      if (i >= n_spec && w[i] != 0.f)                                 // uniform across the warp
+        a[i] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(i) * kHeadDim);
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      if (w[i] != 0.f) {
+        acc.x = fmaf(w[i], a[i].x, acc.x); acc.y = fmaf(w[i], a[i].y, acc.y);
+        acc.z = fmaf(w[i], a[i].z, acc.z); acc.w = fmaf(w[i], a[i].w, acc.w);
       }
     }
   }
+  if (groups > 1) {                                 // one row per CTA
+    if (g > 0) xfer[((g - 1) * 2 + part) * 32 + lane] = acc;
+    __syncthreads();
+    if (g > 0) return;
+    for (int h = 1; h < groups; ++h) {
+      const float4 v = xfer[((h - 1) * 2 + part) * 32 + lane];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+  }
+  if (!live || g > 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const int64_t tok = row / p.num_q_heads, head = row - tok * p.num_q_heads;
   __nv_bfloat16* dst = p.out + tok * p.out_stride_tok + head * p.out_stride_head + part * 128 + lane * 4;
@@ -97,17 +117,19 @@ attn_reduce_kernel(const AttnParams p) {
 
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
+  const int groups = (p.num_segments + kGroup - 1) / kGroup;
+  const int rows_per_cta = groups == 1 ? 2 : 1;    // 128 threads for S <= 16, else 64 per group
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows * kWarpsPerRow + kWarpsPerCta - 1) / kWarpsPerCta));
-  cfg.blockDim = dim3(kWarpsPerCta * 32);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
+  cfg.blockDim = dim3(rows_per_cta * 2 * groups * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(groups - 1) * 2 * 32 * sizeof(float4);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_reduce_kernel, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_reduce_kernel, p, groups, rows_per_cta);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

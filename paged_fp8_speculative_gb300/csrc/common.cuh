@@ -1,6 +1,7 @@
 // Shared definitions of the CUDA path (kernels and host launchers).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -31,9 +32,10 @@ struct AttnParams {
   const float* v_descale;
   float scale_log2;     // softmax_scale * log2(e): logits are kept in the log2 domain
   int32_t num_segments;
-  int32_t slots_used;    // slots the main kernel may write per row (<= num_segments); set by its launcher
+  int32_t slots_used;    // slots most rows use (<= num_segments): the reduce loads them with the LSEs
   uint32_t* tile_ctr;    // per-unit tile counters (workspace header; zero between calls)
   int32_t deterministic; // 1: fixed page ranges per piece (bit-identical repeats)
+  int32_t scheduling;    // 0: chunks sized for max_pages, 1: pieces planned from the lengths
   float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
   float* lse_part;      // [total_q * H_q][S] float32, log2-sum-exp2 of the segment (NaN = error)
   __nv_bfloat16* out;
@@ -63,8 +65,17 @@ __device__ inline void set_status(int32_t* status, int bits) {
 constexpr int kMaxTileCounters = 1024;
 constexpr size_t kWorkspaceHeaderBytes = kMaxTileCounters * sizeof(uint32_t);
 
+// Planned scheduling handles at most this many (sequence, KV head) units (8 per lane of the
+// planning warp), and no more units than SMs.
+constexpr int kPlanUnits = 256;
+
+// The main kernel: chunked scheduling (attn_main_tc.cu), or planned scheduling
+// (attn_main_planned.cu) when p.scheduling asks for it and the batch allows it.
 cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_main_planned(AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
+// Tensor maps of the K and V caches (cached per cache, pool size and device).
+bool kv_tensor_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* mv);
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, int blocks,
                                cudaStream_t stream);
 int device_sm_count(int device);

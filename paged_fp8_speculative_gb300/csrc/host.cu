@@ -29,6 +29,7 @@ int device_sm_count(int device) {
 namespace {
 
 std::atomic<int> g_deterministic{0};   // scheduling switch, see mtp_verify_attn_set_deterministic
+std::atomic<int> g_scheduling{0};      // see mtp_verify_attn_set_scheduling
 
 constexpr size_t kAlign = 256;
 
@@ -166,6 +167,7 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   p.out_stride_head = out_stride_head;
   p.status = status;
   p.deterministic = g_deterministic.load(std::memory_order_relaxed);
+  p.scheduling = g_scheduling.load(std::memory_order_relaxed);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_attn_main(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
@@ -175,6 +177,12 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
 
 extern "C" void mtp_verify_attn_set_deterministic(int32_t on) { g_deterministic.store(on ? 1 : 0); }
 extern "C" int32_t mtp_verify_attn_get_deterministic(void) { return g_deterministic.load(); }
+extern "C" int32_t mtp_verify_attn_set_scheduling(int32_t mode) {
+  if (mode != MTPATTN_SCHED_CHUNKED && mode != MTPATTN_SCHED_PLANNED) return MTPATTN_E_ARG;
+  g_scheduling.store(mode);
+  return MTPATTN_OK;
+}
+extern "C" int32_t mtp_verify_attn_get_scheduling(void) { return g_scheduling.load(); }
 
 extern "C" const char* mtp_verify_attn_strerror(int status) {
   switch (status) {

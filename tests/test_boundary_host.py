@@ -136,3 +136,15 @@ def test_deterministic_switch():
     finally:
         api.mtp_verify_attn_set_deterministic(False)
     assert not api.mtp_verify_attn_get_deterministic()
+
+
+def test_scheduling_switch():
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
+    api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+    try:
+        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+        assert _lib.lib().mtp_verify_attn_set_scheduling(2) == api.E_ARG
+        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+    finally:
+        api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED

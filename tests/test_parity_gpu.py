@@ -27,6 +27,14 @@ pytestmark = pytest.mark.gpu
 TOL = 0.01
 
 
+@pytest.fixture(params=[api.SCHED_CHUNKED, api.SCHED_PLANNED], ids=["chunked", "planned"])
+def sched(request):
+    """Run the test under both ways of laying out the pieces."""
+    api.mtp_verify_attn_set_scheduling(request.param)
+    yield request.param
+    api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
+
+
 def run_gpu(batch, num_segments=None, status=None, block_tables=None, out=None, q=None):
     d = batch
     kd = torch.tensor([d.k_descale], dtype=torch.float32, device="cuda")
@@ -71,17 +79,17 @@ CASES = {
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_parity_against_oracle(name):
+def test_parity_against_oracle(name, sched):
     check(CASES[name]())
 
 
 @pytest.mark.parametrize("S", [1, 2, 3, 5, 16, 63, 64])
-def test_any_segment_count_matches_oracle(S):
+def test_any_segment_count_matches_oracle(S, sched):
     check(synth.make_batch([1000, 345, 80], [4, 2, 3], 16, 1, seed=20 + S, k_descale=0.5,
                            v_descale=2.0), num_segments=S)
 
 
-def test_segment_count_invariance_uniform_keys():
+def test_segment_count_invariance_uniform_keys(sched):
     """All keys equal => the exact output is the mean of the visible V rows.  Every
     segment count must give the same result up to float32 re-association; a
     missed or double-counted page would move it by far more."""
@@ -132,7 +140,7 @@ def test_strided_q_and_out_views():
     assert big_o[:, 0].abs().max().item() == 0
 
 
-def test_repeatable_and_graph_replay_bit_identical():
+def test_repeatable_and_graph_replay_bit_identical(sched):
     """Deterministic scheduling: repeated calls and a graph replay are bit-identical."""
     api.mtp_verify_attn_set_deterministic(True)
     try:
@@ -174,7 +182,7 @@ def _repeatable_and_graph_replay():
     assert not torch.equal(out, eager)
 
 
-def test_balanced_scheduling_repeats_within_reassociation():
+def test_balanced_scheduling_repeats_within_reassociation(sched):
     """Balanced scheduling (the default) lets the pieces of a unit share its tiles: the
     split differs from call to call, the result only by float32 re-association, and the
     tile counters in the workspace header are back at zero after every call."""
@@ -201,7 +209,7 @@ def test_balanced_scheduling_repeats_within_reassociation():
         assert np.abs(o - outs[0]).max() <= 2 ** -7 * scale
 
 
-def test_deterministic_mode_matches_oracle():
+def test_deterministic_mode_matches_oracle(sched):
     api.mtp_verify_attn_set_deterministic(True)
     try:
         check(synth.make_batch([5000, 5000, 31], [4, 2, 1], 16, 1, seed=52), num_segments=16)
@@ -209,7 +217,7 @@ def test_deterministic_mode_matches_oracle():
         api.mtp_verify_attn_set_deterministic(False)
 
 
-def test_device_errors_set_status_and_zero_rows():
+def test_device_errors_set_status_and_zero_rows(sched):
     # Rows of the valid sequences are compared bit for bit across calls: fixed page ranges.
     api.mtp_verify_attn_set_deterministic(True)
     try:
@@ -242,6 +250,29 @@ def _device_errors():
     assert torch.equal(o3[:4], o[:4]) and torch.equal(o3[8:], o[8:])
 
 
+@pytest.mark.parametrize("det", [False, True])
+def test_planned_start_with_wide_block_table(det):
+    """Planned scheduling guesses each CTA's piece from max_pages before it has read the
+    lengths.  With a block table twice as wide as the sequences need, the guess gets the unit
+    and its Q rows right but (with fixed page ranges) not the first tile: the speculative K
+    tile must be dropped and the right one loaded."""
+    api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+    api.mtp_verify_attn_set_deterministic(det)
+    try:
+        for S in (4, 16):
+            check(synth.make_batch([3000] * 6, 4, 16, 1, seed=80 + S, max_pages=376,
+                                   k_descale=0.5, v_descale=2.0), num_segments=S)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+        api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
+
+
+def test_scheduling_switch_refuses_unknown_modes():
+    with pytest.raises(ValueError):
+        api.mtp_verify_attn_set_scheduling(7)
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
+
+
 def test_host_pointers_are_refused():
     batch = synth.make_batch([100], 4, 16, 1, seed=70)
     gb = batch.to("cuda")
@@ -267,7 +298,7 @@ def test_num_segments_heuristic_on_device():
 @pytest.mark.parametrize("name,S", [("verify_16x35k_gqa16", 16), ("verify_16x35k_gqa8", 16),
                                     ("verify_4x35k_gqa16", 64), ("verify_16x70k_gqa16", 16),
                                     ("draft_extend_8", 0), ("decode_8", 0)])
-def test_full_size_sampled_against_oracle(name, S):
+def test_full_size_sampled_against_oracle(name, S, sched):
     """The benchmark shapes at full size, in the launch configuration the bench
     times, checked on sampled sequences the oracle computes one by one."""
     batch = synth.workload(name, seed=1, device="cuda")
