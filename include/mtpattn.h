@@ -187,12 +187,13 @@ int32_t mtp_verify_attn_get_deterministic(void);
 
 /*
  * How the split-KV pieces are laid out over the SMs (process-wide switch):
- *  - MTPATTN_SCHED_CHUNKED (the default): from the host-side shape alone, every
- *    (sequence, KV head) unit is cut as if it held max_pages pages.  Best when the
- *    batch's lengths are close to max_pages; short sequences leave their SMs idle.
- *  - MTPATTN_SCHED_PLANNED (at most 256 units, no more units than SMs): the main
- *    kernel reads seq_lens first and gives each unit a number of pieces in
- *    proportion to its length, so ragged batches keep every SM streaming.
+ *  - MTPATTN_SCHED_PLANNED (the default; used when the batch has at most 256
+ *    (sequence, KV head) units and no more units than SMs, else chunked): the
+ *    main kernel first reads seq_lens and gives each unit a number of pieces in
+ *    proportion to its length, so ragged batches keep every SM streaming.  With
+ *    equal lengths it lays the pieces out exactly as chunked scheduling does.
+ *  - MTPATTN_SCHED_CHUNKED: from the host-side shape alone, every unit is cut as
+ *    if it held max_pages pages; short sequences leave their SMs idle.
  * Returns MTPATTN_E_ARG for an unknown mode.  Thread-safe; takes effect at the
  * next launch.
  */

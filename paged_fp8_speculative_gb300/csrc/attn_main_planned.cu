@@ -1,10 +1,10 @@
 // Split-KV main kernel with planned scheduling (tcgen05, TMA, TMEM on the sm_100 family).
 //
 // The roles, the hi/lo e4m3 precision scheme, the TMEM layout and the online softmax are
-// those of the chunked kernel in attn_main_tc.cu; this file differs in how pieces are laid
-// out and in how a CTA starts.  The two live in separate files because the hot loops of the
-// chunked kernel measurably lose speed when this file's start-up logic is compiled into the
-// same kernel (a few percent at 16 x 35k tokens), so each kernel is compiled on its own.
+// those of the chunked kernel in attn_main_tc.cu, and so are its per-role loops; this file
+// differs in how pieces are laid out and in how a CTA finds its piece.  The two kernels are
+// compiled from separate files: with both ways of scheduling in one source (a template over
+// the scheduling) the hot loops ran measurably slower, a few percent at 16 x 35k tokens.
 //
 // Scheduling.  The chunked kernel cuts every (sequence, KV head) unit as if it held
 // max_pages pages, which leaves SMs idle on ragged batches.  Here the kernel first reads
@@ -15,11 +15,6 @@
 // then slot 1, ...) so that every unit is spread over the whole GPU.  The pieces of a unit share
 // its tiles through the per-unit counter (as in the chunked kernel), or keep fixed page ranges
 // [s C, (s + 1) C) in deterministic mode; the unit's last piece marks its unused slots empty.
-//
-// Speculative start.  The plan costs a round trip to memory before any K tile could be
-// requested.  The V producer, idle until then, guesses the plan of equal lengths (known from
-// max_pages alone) and requests that piece's Q rows and first K tile at once; the plan then
-// keeps them or they are dropped (see the producers).
 //
 // The kernel is launched as a programmatic dependent of the previous work on the stream and
 // lets the split-KV reduce be scheduled as soon as it starts.
@@ -87,12 +82,9 @@ struct Bars {
   int32_t tid[kRing];               // first page of the piece's next tile, or -1: piece done
   uint32_t tmem_base;
   int32_t abort;
-  uint64_t plan_ready;              // planned scheduling: the CTA's piece is in plan_*
-  uint64_t k_spec_full;             // speculative first K tile (into K slot 0) has landed
-  uint64_t q_spec_land;             // speculative Q rows have landed in the Q buffer
+  uint64_t plan_ready;              // the CTA's piece is in plan_* (written by the K producer)
   int64_t plan_k, plan_u;
   int32_t plan_s, plan_pu, plan_C, plan_b, plan_h, plan_L, plan_q0, plan_q1;
-  int32_t k_spec, q_spec;           // the plan kept the speculative K tile / Q rows
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -471,14 +463,10 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
     mbar_init(smem_u32(&bars.q_land), 1);
     mbar_init(smem_u32(&bars.q_free), 1);
     mbar_init(smem_u32(&bars.plan_ready), 1);
-    mbar_init(smem_u32(&bars.k_spec_full), 1);
-    mbar_init(smem_u32(&bars.q_spec_land), 1);
     mbar_init(smem_u32(&bars.xbar[0]), kSoftmaxThreads);
     mbar_init(smem_u32(&bars.xbar[1]), kSoftmaxThreads);
     for (int i = 0; i < kRing; ++i) mbar_init(smem_u32(&bars.tid_full[i]), 1);
     bars.abort = 0;
-    bars.k_spec = 0;
-    bars.q_spec = 0;
     fence_mbar_init();
   }
   // The V ring must hold finite values before any P = 0 column meets it.
@@ -496,12 +484,30 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
   // The segment reduce may be scheduled now; it waits for this grid's results itself.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-  // The CTA's first cursor.  Planned scheduling: the K producer warp plans (see there) and
-  // publishes the plan; the other warps take it from shared memory.
-  Cursor plan_c;                       // K producer warp: its plan
+  // The CTA's piece.  The K producer warp plans and publishes the plan; the other warps take
+  // it from shared memory.
   auto first_cursor = [&]() -> Cursor {
     Cursor c;
-    if (warp == 0) return plan_c;
+    if (warp == 0) {
+      PlanIn in;
+      plan_load(prm, lane, in);
+      c = plan_piece(prm, lane, in);
+      if (lane == 0) {
+        bars.plan_k = c.k;
+        bars.plan_u = c.u;
+        bars.plan_s = c.s;
+        bars.plan_pu = c.pu;
+        bars.plan_C = c.C;
+        bars.plan_b = c.b;
+        bars.plan_h = c.h;
+        bars.plan_L = c.L;
+        bars.plan_q0 = c.q0;
+        bars.plan_q1 = c.q1;
+        mbar_arrive(smem_u32(&bars.plan_ready));
+      }
+      __syncwarp();
+      return c;
+    }
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.plan_ready), 0, abort_flag));
     c.k = ok ? bars.plan_k : prm.num_chunks;
     c.u = bars.plan_u;
@@ -529,112 +535,7 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
     uint32_t e = 0;    // entries of the tile-sequence ring passed (tiles and end marks)
     uint32_t n_q = 0;  // pieces whose Q rows this (K) producer has copied
     bool stop = false;
-    uint32_t n_qf = 0; // pieces whose Q rows were placed in the Q buffer (q_free parity)
-    // Q rows of a piece: row r (token r / ratio, head h * ratio + r % ratio) to byte r * 512 of
-    // the Q buffer, completing on `bar`.  Each copy instruction costs the TMA unit tens of
-    // cycles, so when the heads of a token are contiguous (the usual layout) one copy moves all
-    // `ratio` rows of a token.
-    auto issue_q = [&](int q0, int ql, int h, uint32_t bar) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, ql * p.ratio * 2 * kHeadDim);
-      __syncwarp();
-      if (p.q_stride_head == kHeadDim) {
-        if (lane < ql)
-          bulk_load(smem_u32(base + kOffQ + lane * p.ratio * 2 * kHeadDim),
-                    p.q + static_cast<int64_t>(q0 + lane) * p.q_stride_tok +
-                        static_cast<int64_t>(h) * p.ratio * kHeadDim,
-                    p.ratio * 2 * kHeadDim, bar);
-      } else {
-        for (int r = lane; r < ql * p.ratio; r += 32) {
-          const int tk = r / p.ratio, g = r - tk * p.ratio;
-          const __nv_bfloat16* src = p.q + static_cast<int64_t>(q0 + tk) * p.q_stride_tok +
-                                     static_cast<int64_t>(h * p.ratio + g) * p.q_stride_head;
-          bulk_load(smem_u32(base + kOffQ + r * 2 * kHeadDim), src, 2 * kHeadDim, bar);
-        }
-      }
-    };
-    // Planned scheduling: the plan needs the lengths (one round trip), and the piece's first
-    // K tile and Q rows need its block-table and cu_seqlens_q entries (another).  To overlap the
-    // two, the piece this CTA gets when every unit has max_pages pages (the plan of equal
-    // lengths, known without any load) is guessed.  The V producer, idle until the plan is
-    // known, requests the guess's Q rows (on q_spec_land) and first K tile (into K slot 0, on
-    // k_spec_full) while the K producer plans.  The plan then keeps them, and the roles that
-    // read them wait on those barriers, or they are left to land and dropped.
-    bool k_sent = false, q_sent = false;   // speculative copies issued (both producers know)
-    bool k_kept = false, q_kept = false;   // ... and kept by the plan
-    bool k0_open = false;                  // kept K tile: k_full[0] phase 0 still to complete
-    {
-      const int B = p.num_seqs, U = B * p.num_kv_heads, V = p.max_pages;
-      const int k = blockIdx.x;
-      const bool guess = k < U * prm.g_pu;
-      int g_b = 0, g_h = 0, g_pg = 0, g_np = 0, g_q0 = 0, g_q1 = 0, g_phys = 0;
-      if (guess) {
-        const int ks = div_inv(k, U, prm.inv_units), ku = k - ks * U;
-        g_h = div_inv(ku, B, prm.inv_seqs);
-        g_b = ku - g_h * B;
-        g_pg = prm.shared_tiles ? ks * kPagesPerTile : ks * prm.g_C;
-        g_np = prm.shared_tiles ? min(kPagesPerTile, V - g_pg)
-                                : min(min(kPagesPerTile, prm.g_C), V - g_pg);
-        if (is_v && lane < g_np) g_phys = p.block_tables[static_cast<size_t>(g_b) * V + g_pg + lane];
-        g_q0 = p.cu_q[g_b];
-        g_q1 = p.cu_q[g_b + 1];
-      }
-      PlanIn in;
-      if (!is_v) plan_load(prm, lane, in);
-      const int g_ql = g_q1 - g_q0;
-      q_sent = guess && g_q0 >= 0 && g_q1 <= p.total_q && g_ql >= 1 && g_ql <= kMaxQLen;
-      k_sent = guess && g_np > 0;
-      if (is_v) {
-        if (q_sent) issue_q(g_q0, g_ql, g_h, smem_u32(&bars.q_spec_land));
-        if (k_sent) {
-          if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars.k_spec_full), g_np * 2 * 2048);
-          __syncwarp();
-          if (lane < g_np) {
-            const uint32_t dst = smem_u32(base + kOffK);
-            tma_load_4d(dst + lane * 2048, &prm.tmap_k, smem_u32(&bars.k_spec_full), 0, g_h, 0,
-                        g_phys, pol);
-            tma_load_4d(dst + kHalfBytes + lane * 2048, &prm.tmap_k, smem_u32(&bars.k_spec_full),
-                        128, g_h, 0, g_phys, pol);
-          }
-        }
-      } else {
-        plan_c = plan_piece(prm, lane, in);
-        if (plan_c.k < prm.num_chunks) {
-          const Item y = item_info(prm, plan_c, lane);
-          if (y.ntiles > 0 && y.b == g_b && y.h == g_h) {
-            q_kept = q_sent && y.q0 == g_q0 && y.ql == g_ql;
-            const int i0 = prm.shared_tiles ? y.s : 0;    // the piece's first tile
-            const int pg0 = y.pb + i0 * kPagesPerTile;
-            k_kept = k_sent && i0 < y.ntiles && pg0 == g_pg && min(kPagesPerTile, y.pe - pg0) == g_np;
-          }
-        }
-        if (lane == 0) {
-          bars.plan_k = plan_c.k;
-          bars.plan_u = plan_c.u;
-          bars.plan_s = plan_c.s;
-          bars.plan_pu = plan_c.pu;
-          bars.plan_C = plan_c.C;
-          bars.plan_b = plan_c.b;
-          bars.plan_h = plan_c.h;
-          bars.plan_L = plan_c.L;
-          bars.plan_q0 = plan_c.q0;
-          bars.plan_q1 = plan_c.q1;
-          bars.k_spec = k_kept;
-          bars.q_spec = q_kept;
-          mbar_arrive(smem_u32(&bars.plan_ready));
-          // A dropped copy must land before its buffer is refilled.
-          volatile int no_abort = 0;
-          if (k_sent && !k_kept) mbar_wait(smem_u32(&bars.k_spec_full), 0, &no_abort);
-          if (q_sent && !q_kept) mbar_wait(smem_u32(&bars.q_spec_land), 0, &no_abort);
-        }
-        __syncwarp();
-        k0_open = k_kept;
-        if (q_kept) n_qf = 1;
-      }
-    }
-    bool q_pre = q_kept;                   // the first piece's Q rows are the kept ones
-    const Cursor c0 = first_cursor();
-    if (is_v) k_kept = bars.k_spec;   // set before the plan was published
-    for (Cursor cur = c0; cur.k < prm.num_chunks && !stop && !*abort_flag; cur = cursor_next(prm, cur)) {
+    for (Cursor cur = first_cursor(); cur.k < prm.num_chunks && !stop && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
       if (x.ntiles == 0) continue;
       const int32_t* bt = p.block_tables + static_cast<size_t>(x.b) * p.max_pages;
@@ -643,19 +544,30 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
       // stopped reading that buffer.  Each copy instruction costs the TMA unit tens of
       // cycles, so when the heads of a token are contiguous (the usual layout) one copy
       // moves all `ratio` rows of a token.
-      // The piece's Q rows (K producer only), once the previous piece's last QK has stopped
-      // reading the Q buffer; not for a piece whose rows the plan kept.
-      const bool q_here = !q_pre;
-      q_pre = false;
       auto copy_q = [&]() -> bool {
-        if (!q_here) return true;
         bool q_ok = true;
-        if (lane == 0) q_ok = mbar_wait(smem_u32(&bars.q_free), (n_qf & 1) ^ 1, abort_flag);
+        if (lane == 0) {
+          q_ok = mbar_wait(smem_u32(&bars.q_free), (n_q & 1) ^ 1, abort_flag);
+          if (q_ok) mbar_arrive_expect_tx(smem_u32(&bars.q_land), x.R * 2 * kHeadDim);
+        }
         q_ok = __shfl_sync(0xffffffffu, q_ok, 0);
         if (!q_ok) return false;
-        issue_q(x.q0, x.ql, x.h, smem_u32(&bars.q_land));
+        if (p.q_stride_head == kHeadDim) {
+          if (lane < x.ql)
+            bulk_load(smem_u32(base + kOffQ + lane * p.ratio * 2 * kHeadDim),
+                      p.q + static_cast<int64_t>(x.q0 + lane) * p.q_stride_tok +
+                          static_cast<int64_t>(x.h) * p.ratio * kHeadDim,
+                      p.ratio * 2 * kHeadDim, smem_u32(&bars.q_land));
+        } else {
+          for (int r = lane; r < x.R; r += 32) {
+            const int tk = r / p.ratio, g = r - tk * p.ratio;
+            const __nv_bfloat16* src = p.q + static_cast<int64_t>(x.q0 + tk) * p.q_stride_tok +
+                                       static_cast<int64_t>(x.h * p.ratio + g) * p.q_stride_head;
+            bulk_load(smem_u32(base + kOffQ + r * 2 * kHeadDim), src, 2 * kHeadDim,
+                      smem_u32(&bars.q_land));
+          }
+        }
         ++n_q;
-        ++n_qf;
         return true;
       };
       // The piece's tile sequence is decided by the K producer and handed to every other
@@ -710,41 +622,32 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
         const int st = t % kStages;
         // One page per lane, loads in parallel.  The first tile's address comes from the
         // cursor alone, so its entries are fetched together with the piece's lengths.
-        const bool kept = !is_v && t == 0 && k_kept;   // already in K slot 0 (speculative copy)
-        const int pg_first = x.vp0;
+        const int pg_first = prm.shared_tiles ? x.s * kPagesPerTile : x.vp0;
         const int pg_spec = (j == 0 ? pg_first : pg0) + lane;
-        int phys = (!kept && lane < kPagesPerTile && pg_spec < p.max_pages) ? bt[pg_spec] : 0;
+        int phys = (lane < kPagesPerTile && pg_spec < p.max_pages) ? bt[pg_spec] : 0;
         if (lane >= np) phys = 0;
         const uint32_t fb = smem_u32(&full[st]);
         bool ok = true;
         if (lane == 0) {
           // Start-up: the first K tile goes out ahead of the other K tiles (and of every V
           // tile), so that it is not queued behind them.
-          // A kept speculative tile completes k_full[0] phase 0 here, once it has landed.
-          if (t == 1 && !is_v && k0_open) {
-            ok = mbar_wait(smem_u32(&bars.k_spec_full), 0, abort_flag);
-            if (ok) mbar_arrive(smem_u32(&bars.k_full[0]));
-          } else if (t == 0 && is_v && k_kept) {
-            ok = mbar_wait(smem_u32(&bars.k_spec_full), 0, abort_flag);
-          } else if ((t == 1 && !is_v) || (t == 0 && is_v)) {
+          if ((t == 1 && !is_v) || (t == 0 && is_v))
             ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, abort_flag);
-          }
           ok = ok && mbar_wait(smem_u32(&empty[st]), ((t / kStages) & 1) ^ 1, abort_flag);
           if (ok) {
             if (!is_v) {                       // published once its K slot is free (ring bound)
               bars.tid[e % kRing] = pg0;
               mbar_arrive(smem_u32(&bars.tid_full[e % kRing]));
             }
-            if (!kept) mbar_arrive_expect_tx(fb, np * 2 * 2048);
+            mbar_arrive_expect_tx(fb, np * 2 * 2048);
           }
         }
-        if (t == 1 && !is_v) k0_open = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           stop = true;
           break;
         }
-        if (lane < np && !kept) {
+        if (lane < np) {
           const uint32_t dst = smem_u32(base + ring + st * kTileBytes);
           tma_load_4d(dst + lane * 2048, map, fb, 0, x.h, 0, phys, pol);
           tma_load_4d(dst + kHalfBytes + lane * 2048, map, fb, 128, x.h, 0, phys, pol);
@@ -757,22 +660,16 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
           break;
         }
       }
-      if (!is_v && k0_open) {                  // a one-tile piece never reached the gate above
-        if (lane == 0 && mbar_wait(smem_u32(&bars.k_spec_full), 0, abort_flag))
-          mbar_arrive(smem_u32(&bars.k_full[0]));
-        k0_open = false;
-        __syncwarp();
-      }
     }
     // Never leave with copies in flight: wait for the last Q rows and the last issued tiles.
-    if (lane == 0) {
+    if (lane == 0 && n_q > 0) {
       volatile int no_abort = 0;
-      if (n_q > 0) mbar_wait(smem_u32(&bars.q_land), (n_q - 1) & 1, &no_abort);
-      if (q_sent) mbar_wait(smem_u32(&bars.q_spec_land), 0, &no_abort);
-      if (k_sent) mbar_wait(smem_u32(&bars.k_spec_full), 0, &no_abort);
+      mbar_wait(smem_u32(&bars.q_land), (n_q - 1) & 1, &no_abort);
+    }
+    if (lane == 0) {
       for (uint32_t k = 0; k < kStages && k < t; ++k) {
         const uint32_t u = t - 1 - k;
-        if (u == 0 && k_kept && !is_v) continue;   // K slot 0 was filled by the speculative copy
+        volatile int no_abort = 0;
         mbar_wait(smem_u32(&full[u % kStages]), (u / kStages) & 1, &no_abort);
       }
     }
@@ -811,9 +708,7 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
       return true;
     };
     uint32_t e = 0;                            // tile-sequence ring entries passed
-    const Cursor c0 = first_cursor();
-    const bool k_kept = bars.k_spec;   // set before the plan was published
-    for (Cursor cur = c0; cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
+    for (Cursor cur = first_cursor(); cur.k < prm.num_chunks && !*abort_flag; cur = cursor_next(prm, cur)) {
       const Item x = item_info(prm, cur, lane);
       if (x.ntiles == 0) continue;
       bool ok = wait_all(bars.q_ready, items_run & 1);
@@ -829,12 +724,7 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
         // S buffer u & 1 still holds P(u - 2) for PV(u - 2).  That PV was issued before this
         // QK by this warp, and MMAs of one thread execute in issue order, so it reads P(u - 2)
         // before QK(u) overwrites it: no wait on its completion is needed.
-        // The first tile may be the speculative copy the plan kept (its own barrier).
-        const bool kept = u == 0 && k_kept;
-        if (!wait_all(kept ? bars.k_spec_full : bars.k_full[st], kept ? 0u : (u / kStages) & 1)) {
-          ok = false;
-          break;
-        }
+        if (!wait_all(bars.k_full[st], (u / kStages) & 1)) { ok = false; break; }
         tc_fence_after();
         if (leader) {
 #pragma unroll
@@ -934,15 +824,9 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
     // sit in warp (quad, half ^ 1): the exchange gives it, and since every thread arrives
     // only after its reads, it also frees the buffer for the codes that overwrite it.
     uint32_t q_par = 0;
-    bool q_pre = false;                        // the first piece's Q rows came speculatively
     auto prepare_q = [&](const Item& y, int& a_exp_row) -> bool {
-      if (q_pre) {                             // the plan kept the speculative copy
-        q_pre = false;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.q_spec_land), 0, abort_flag))) return false;
-      } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.q_land), q_par, abort_flag))) return false;
-        q_par ^= 1;
-      }
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.q_land), q_par, abort_flag))) return false;
+      q_par ^= 1;
       int a_exp = 0;
       const bool valid = q_row < y.R;
       const int part = q_is_hi ? 0 : 1;
@@ -1001,7 +885,6 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
     uint32_t e = 0;                            // tile-sequence ring entries passed
     Item x;
     Cursor it = next_running(first_cursor(), x);
-    q_pre = bars.q_spec;           // set before the plan was published
     int a_exp = 0;
     bool alive = it.k >= prm.num_chunks || prepare_q(x, a_exp);
     while (alive && it.k < prm.num_chunks) {
@@ -1223,8 +1106,8 @@ cudaError_t launch_attn_main_planned(AttnParams& p, cudaStream_t stream) {
   // slots with the LSEs and the others only if a unit used them.
   const int64_t per = std::min<int64_t>(S, prm.num_chunks / U);
   p.slots_used = static_cast<int32_t>(per);
-  // The plan of equal lengths (every unit max_pages pages), for the speculative start and as
-  // the plan's fast path; reciprocals for exact small divisions on the device.
+  // The plan of equal lengths (every unit max_pages pages), the plan's fast path; reciprocals
+  // for exact small divisions on the device.
   const int64_t Cg = std::max<int64_t>((V + per - 1) / per, std::min<int64_t>(kPagesPerTile, V));
   prm.g_per = static_cast<int32_t>(per);
   prm.g_C = static_cast<int32_t>(Cg);

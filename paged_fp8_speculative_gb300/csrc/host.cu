@@ -29,7 +29,7 @@ int device_sm_count(int device) {
 namespace {
 
 std::atomic<int> g_deterministic{0};   // scheduling switch, see mtp_verify_attn_set_deterministic
-std::atomic<int> g_scheduling{0};      // see mtp_verify_attn_set_scheduling
+std::atomic<int> g_scheduling{MTPATTN_SCHED_PLANNED};   // see mtp_verify_attn_set_scheduling
 
 constexpr size_t kAlign = 256;
 

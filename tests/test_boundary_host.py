@@ -139,12 +139,12 @@ def test_deterministic_switch():
 
 
 def test_scheduling_switch():
-    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
-    api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED      # the default
+    api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
     try:
-        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
         assert _lib.lib().mtp_verify_attn_set_scheduling(2) == api.E_ARG
-        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+        assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
     finally:
-        api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
-    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
+        api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED

@@ -32,7 +32,7 @@ def sched(request):
     """Run the test under both ways of laying out the pieces."""
     api.mtp_verify_attn_set_scheduling(request.param)
     yield request.param
-    api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
+    api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
 
 
 def run_gpu(batch, num_segments=None, status=None, block_tables=None, out=None, q=None):
@@ -251,12 +251,10 @@ def _device_errors():
 
 
 @pytest.mark.parametrize("det", [False, True])
-def test_planned_start_with_wide_block_table(det):
-    """Planned scheduling guesses each CTA's piece from max_pages before it has read the
-    lengths.  With a block table twice as wide as the sequences need, the guess gets the unit
-    and its Q rows right but (with fixed page ranges) not the first tile: the speculative K
-    tile must be dropped and the right one loaded."""
-    api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+def test_planned_with_wide_block_table(det):
+    """Planned scheduling with a block table twice as wide as the sequences need: the plan
+    sizes the pieces from the lengths (not from max_pages), in both tile-sharing and
+    fixed-range mode."""
     api.mtp_verify_attn_set_deterministic(det)
     try:
         for S in (4, 16):
@@ -264,13 +262,12 @@ def test_planned_start_with_wide_block_table(det):
                                    k_descale=0.5, v_descale=2.0), num_segments=S)
     finally:
         api.mtp_verify_attn_set_deterministic(False)
-        api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
 
 
 def test_scheduling_switch_refuses_unknown_modes():
     with pytest.raises(ValueError):
         api.mtp_verify_attn_set_scheduling(7)
-    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_CHUNKED
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
 
 
 def test_host_pointers_are_refused():
