@@ -383,7 +383,9 @@ def run_ours(a) -> None:
         "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms / a.steps, "us_per_call": us_call,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic", "config": workload_config(a) | {"num_segments": S},
+        "data": "synthetic",
+        "config": workload_config(a) | {"num_segments": S, "scheduling": (
+            "planned" if api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED else "chunked")},
         "frac_of_8tbs_nominal": value / world / 8.0,
         "read_ceiling": {"value_gbs": ceiling_gbs, "frac": value / world * 1e3 / ceiling_gbs,
                          "kernel": "mtpattn_stream_read, 16-B loads"},
