@@ -264,6 +264,18 @@ def test_planned_with_wide_block_table(det):
         api.mtp_verify_attn_set_deterministic(False)
 
 
+@pytest.mark.parametrize("nseq,hkv,S", [(100, 1, 16), (70, 2, 4), (150, 1, 2), (40, 4, 64)])
+def test_planned_many_units_ragged(nseq, hkv, S, sched):
+    """Many (sequence, KV head) units with log-uniform lengths: the plan's general path (up to
+    8 units per lane of the planning warp, the binary searches over the piece size and the
+    slots), and with more units than SMs (nseq x hkv = 160) the chunked fallback."""
+    ctx = synth.log_uniform_contexts(nseq, 6, 3000, seed=nseq + hkv)
+    ql = synth.uniform_q_lens(nseq, 1, 4, seed=nseq + 7)
+    ctx = [max(c, q) for c, q in zip(ctx, ql)]
+    check(synth.make_batch(ctx, ql, 8 * hkv, hkv, seed=100 + nseq, kv_recipe="unit",
+                           k_descale=0.5, v_descale=2.0), num_segments=S)
+
+
 def test_scheduling_switch_refuses_unknown_modes():
     with pytest.raises(ValueError):
         api.mtp_verify_attn_set_scheduling(7)
