@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import glob
 import hashlib
+import re
 import json
 import math
 import os
@@ -211,10 +212,16 @@ def hbm_peak() -> tuple[float, str]:
 
 
 def source_digest() -> str:
+    """Digest of the kernel sources with comments and blank space removed, so that a profile
+    summary stays attached to the code it measured when only comments change."""
     h = hashlib.sha256()
     for path in sorted(glob.glob(os.path.join(ROOT, "paged_fp8_speculative_gb300", "csrc", "*"))):
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode() + f.read())
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)        # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                      # line comments
+        text = " ".join(text.split())
+        h.update(os.path.basename(path).encode() + text.encode())
     return h.hexdigest()[:16]
 
 

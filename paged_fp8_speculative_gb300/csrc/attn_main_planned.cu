@@ -96,12 +96,14 @@ struct Cursor {
   int L, q0, q1;           // planned scheduling: the unit's seq_lens and cu_seqlens_q entries
 };
 
-// Planned scheduling (at most kPlanUnits units, no more units than CTAs): every warp of every
-// CTA computes the same plan from the sequence lengths.  Unit v has n_v pages; the chunk is the
-// smallest C >= 8 (one tile) with sum_v ceil(n_v / C) <= grid and ceil(n_v / C) <= S, so the
-// longest sequences get the most CTAs; unit v has p_v = ceil(n_v / C) pieces.  CTAs take the pieces slot-major
-// (slot 0 of every unit, then slot 1, ...), which spreads every unit over the whole grid:
-// neighbouring CTAs tend to share a part of the GPU, and parts stream at different rates.
+// Planned scheduling (at most kPlanUnits units, no more units than CTAs): the K producer warp
+// of every CTA computes the same plan from the sequence lengths.  Unit v has n_v pages; the
+// chunk is the smallest C >= 8 (one tile) with sum_v ceil(n_v / C) <= grid and
+// ceil(n_v / C) <= S, so the longest sequences get the most CTAs; unit v has
+// p_v = ceil(n_v / C) pieces.  CTAs take the pieces slot-major (slot 0 of every unit, then
+// slot 1, ...), which spreads every unit over the whole grid: neighbouring CTAs tend to share a
+// part of the GPU, and parts stream at different rates.
+//
 // ceil(n / c) for 0 <= n < 2^24, 1 <= c, with inv = 1 / c: a float estimate, then made exact.
 __device__ __forceinline__ int ceil_div_inv(int n, int c, float inv) {
   int q = __float2int_rd(static_cast<float>(n + c - 1) * inv);
