@@ -28,9 +28,8 @@ constexpr int kGroup = 16;          // slots per warp
 
 __global__ void __launch_bounds__(256)
 attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
-  // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic,
-  // and none at all for S <= 16, so that the reduce's CTAs fit beside a finishing main-kernel
-  // CTA that still holds nearly all of its SM's shared memory.
+  // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic
+  // shared memory, requested only for S > 16.
   extern __shared__ float4 xfer[];
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   // The next kernel on the stream (the next call's main kernel) may start its set-up now;
