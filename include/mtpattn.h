@@ -81,11 +81,17 @@ extern "C" {
 /*
  * Number of split slots S per (sequence, KV head) for a batch shape, in [1, 64]
  * (aiter PR #5190 page, Modifications: mtp_verify_attn_num_segments(); no
- * formula is printed).  Our rule: the page share of one SM is
- * ceil(num_seqs * num_kv_heads * max_pages_per_seq / SMs); S is the number of
- * shares a full-length unit can touch, ceil(max_pages_per_seq / share) + 1,
- * capped at 64.  device < 0 means the current device.  Returns a negative
- * MTPATTN_E_* on bad arguments or when the device cannot be queried.
+ * formula is printed).  Our rule depends on the scheduling switch below:
+ *  - planned scheduling (and U = num_seqs * num_kv_heads <= 256 and <= SMs):
+ *    S = min(SMs - U + 1, ceil(max_pages_per_seq / 8)), clamped to [1, 64]: the
+ *    pieces are sized from the lengths on the device, and S only caps how many
+ *    SMs one long sequence may take;
+ *  - otherwise: the page share of one SM is
+ *    ceil(num_seqs * num_kv_heads * max_pages_per_seq / SMs), and S is the number
+ *    of shares a full-length unit can touch, ceil(max_pages_per_seq / share) + 1,
+ *    capped at 64.
+ * device < 0 means the current device.  Returns a negative MTPATTN_E_* on bad
+ * arguments or when the device cannot be queried.
  */
 int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
                                      int32_t max_pages_per_seq, int32_t device);

@@ -3,6 +3,8 @@
 // touches device memory contents, so a call can be captured in a CUDA graph.
 #include "common.cuh"
 
+#include <algorithm>
+
 #include <math.h>
 #include <atomic>
 #include <stddef.h>
@@ -58,8 +60,19 @@ extern "C" int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv
   if (num_seqs <= 0 || num_kv_heads <= 0 || max_pages_per_seq <= 0) return MTPATTN_E_ARG;
   const int sms = device_sm_count(device);
   if (sms <= 0) return MTPATTN_E_DEVICE;
-  // Enough split slots for a unit of max_pages_per_seq pages to be cut at every
-  // boundary of an equal per-SM share of the batch's pages.
+  const long long units = static_cast<long long>(num_seqs) * num_kv_heads;
+  if (g_scheduling.load(std::memory_order_relaxed) == MTPATTN_SCHED_PLANNED && units <= kPlanUnits &&
+      units <= sms) {
+    // Planned scheduling sizes the pieces from the lengths, so S only caps the pieces of one
+    // unit: allow a single long sequence every SM the other units leave (one each), but no
+    // piece shorter than one 128-key tile.
+    long long s = std::min<long long>(sms - units + 1, (max_pages_per_seq + 7) / 8);
+    if (s < 1) s = 1;
+    if (s > MTPATTN_MAX_SEGMENTS) s = MTPATTN_MAX_SEGMENTS;
+    return static_cast<int32_t>(s);
+  }
+  // Chunked scheduling: enough split slots for a unit of max_pages_per_seq pages to be cut at
+  // every boundary of an equal per-SM share of the batch's pages.
   const long long V = max_pages_per_seq;
   const long long total = static_cast<long long>(num_seqs) * num_kv_heads * V;
   const long long share = (total + sms - 1) / sms;

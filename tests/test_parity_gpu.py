@@ -295,13 +295,28 @@ def test_host_pointers_are_refused():
 def test_num_segments_heuristic_on_device():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
-    def expect(b, hkv, v):
+    def chunked(b, hkv, v):
         share = -(-(b * hkv * v) // sms)
         return min(64, -(-v // share) + 1)
 
-    for args in ((16, 1, 2188), (1, 1, 3), (1000, 8, 100), (4, 1, 2188), (8, 1, 6563)):
+    def planned(b, hkv, v):
+        u = b * hkv
+        if u > min(256, sms):
+            return chunked(b, hkv, v)
+        return max(1, min(64, sms - u + 1, -(-v // 8)))
+
+    cases = ((16, 1, 2188), (1, 1, 3), (1000, 8, 100), (4, 1, 2188), (8, 1, 6563), (100, 1, 400))
+    assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+    for args in cases:
         s = api.mtp_verify_attn_num_segments(*args)
-        assert 1 <= s <= 64 and s == expect(*args), (args, s)
+        assert 1 <= s <= 64 and s == planned(*args), (args, s)
+    api.mtp_verify_attn_set_scheduling(api.SCHED_CHUNKED)
+    try:
+        for args in cases:
+            s = api.mtp_verify_attn_num_segments(*args)
+            assert 1 <= s <= 64 and s == chunked(*args), (args, s)
+    finally:
+        api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
 
 
 @pytest.mark.parametrize("name,S", [("verify_16x35k_gqa16", 16), ("verify_16x35k_gqa8", 16),
