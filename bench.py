@@ -257,6 +257,22 @@ def workload_config(a) -> dict:
 # --------------------------------------------------------------------------------------------
 # our arm
 
+def slowest_rank(values, device) -> list:
+    """Each rank's timings (ms) reduced to the slowest rank's: the whole job ends when the
+    last replica does."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tbs(kv_bytes_per_rank: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job effective KV-read rate: the KV bytes every rank read in `steps` calls,
+    over the slowest rank's time."""
+    return world * kv_bytes_per_rank * steps / (ms * 1e-3) / 1e12
+
+
 def run_ours(a) -> None:
     import torch
     import torch.distributed as dist
@@ -412,15 +428,13 @@ def run_ours(a) -> None:
         raise RuntimeError(f"end-to-end output differs from the device loop's: {diff} (scale {scale})")
 
     if world > 1:
-        t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+        ms, ms_e2e = slowest_rank([ms, ms_e2e], dev)
         dist.destroy_process_group()
     if rank != 0:
         return
 
     us_call = 1e3 * ms / a.steps
-    value = world * kv_bytes * a.steps / (ms * 1e-3) / 1e12
+    value = job_tbs(kv_bytes, world, a.steps, ms)
     peak, peak_kind = hbm_peak()
     achieved = alg_bytes / (us_call * 1e-6) / 1e9
     traffic = ncu_traffic(a.workload)
@@ -439,7 +453,7 @@ def run_ours(a) -> None:
                      "kernel": "mtp_verify_attn_fwd (main + reduce)",
                      "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_call": alg_bytes},
         "cpu_baseline": cpu_base,
-        "e2e": {"value": world * kv_bytes * a.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TB/s",
+        "e2e": {"value": job_tbs(kv_bytes, world, a.steps, ms_e2e), "unit": "TB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": 1e3 * ms_e2e / a.steps,
                 "pipelining": "one CUDA graph per step (captured from the public call); the next "
