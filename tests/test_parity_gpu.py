@@ -106,7 +106,7 @@ def test_segment_count_invariance_uniform_keys(sched):
         assert np.abs(o - outs[0]).max() <= 2 ** -6 * np.abs(outs[0]).max()
 
 
-def test_underflow_spike_closed_form():
+def test_underflow_spike_closed_form(sched):
     """q[0] = 8, K_0[0] = 14, V_0 = +1, every other V = -1 over 16384 keys:
     exact out = (e^7 - 16383) / (e^7 + 16383) = -0.874524 in every coordinate."""
     n, D = 16384, 256
@@ -127,7 +127,7 @@ def test_underflow_spike_closed_form():
         assert np.abs(o - expect).max() <= 2 ** -8
 
 
-def test_strided_q_and_out_views():
+def test_strided_q_and_out_views(sched):
     batch = synth.make_batch([300, 700], [3, 4], 16, 1, seed=40)
     ref = oracle.verify_attention(*oracle_args(batch))
     gb = batch.to("cuda")

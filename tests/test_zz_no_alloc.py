@@ -41,13 +41,16 @@ def _regular(b, kd, vd, S):
                                    b.cu_seqlens_q, kd, vd, b.softmax_scale, num_segments=S)
 
 
-def test_static_scratch_matches_regular_entry_point_twice():
+@pytest.mark.parametrize("mode", [api.SCHED_PLANNED, api.SCHED_CHUNKED], ids=["planned", "chunked"])
+def test_static_scratch_matches_regular_entry_point_twice(mode):
     # Deterministic scheduling, so the two entry points must agree bit for bit.
     api.mtp_verify_attn_set_deterministic(True)
+    api.mtp_verify_attn_set_scheduling(mode)
     try:
         _static_vs_regular()
     finally:
         api.mtp_verify_attn_set_deterministic(False)
+        api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
 
 
 def _static_vs_regular():
