@@ -276,6 +276,17 @@ def test_planned_many_units_ragged(nseq, hkv, S, sched):
                            k_descale=0.5, v_descale=2.0), num_segments=S)
 
 
+@pytest.mark.parametrize("nseq,hkv,S", [(300, 1, 8), (200, 4, 3), (200, 4, 1)])
+def test_many_units_chunked_pieces(nseq, hkv, S, sched):
+    """More units than SMs: both switches run the chunked kernel, whose persistent CTAs walk
+    several units each and whose chunks straddle unit boundaries."""
+    ctx = synth.log_uniform_contexts(nseq, 6, 1500, seed=nseq + hkv)
+    ql = synth.uniform_q_lens(nseq, 1, 4, seed=nseq + 7)
+    ctx = [max(c, q) for c, q in zip(ctx, ql)]
+    check(synth.make_batch(ctx, ql, 8 * hkv, hkv, seed=100 + nseq, kv_recipe="unit",
+                           k_descale=0.5, v_descale=2.0), num_segments=S)
+
+
 def test_scheduling_switch_refuses_unknown_modes():
     with pytest.raises(ValueError):
         api.mtp_verify_attn_set_scheduling(7)
