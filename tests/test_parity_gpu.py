@@ -127,6 +127,31 @@ def test_underflow_spike_closed_form(sched):
         assert np.abs(o - expect).max() <= 2 ** -8
 
 
+def test_page_permutation_is_bit_identical(sched):
+    """Moving every page to another place in the pool and rewriting the block table to match
+    leaves the output bit for bit unchanged (fixed page ranges, so the summation order is
+    the same): the kernel reads exactly the pages the table names."""
+    batch = synth.make_batch([1000, 345, 80, 4099], [4, 2, 3, 1], 16, 1, seed=40, spare_pages=37,
+                             k_descale=0.5, v_descale=2.0)
+    n = batch.k_cache.shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(41))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(n)
+    moved = synth.PagedBatch(batch.q, batch.k_cache[perm], batch.v_cache[perm],
+                             torch.where(batch.block_tables >= 0, inv[batch.block_tables.long().clamp(min=0)].int(),
+                                         batch.block_tables),
+                             batch.seq_lens, batch.cu_seqlens_q, batch.k_descale, batch.v_descale,
+                             batch.softmax_scale, batch.num_kv_heads, 16)
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        for S in (1, 7, 16):
+            a = run_gpu(batch.to("cuda"), S)
+            b = run_gpu(moved.to("cuda"), S)
+            assert torch.equal(a, b), S
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
 def test_strided_q_and_out_views(sched):
     batch = synth.make_batch([300, 700], [3, 4], 16, 1, seed=40)
     ref = oracle.verify_attention(*oracle_args(batch))
