@@ -77,14 +77,19 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
     wsum = w0 + w1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    // All the weights first, then every remaining load of the group at once: with the loads
+    // in the loop that shuffles the weights out, each waited for the shuffles before it, and
+    // rows of many slots paid for that in latency.
     float w[kGroup];
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
       const int s2 = s_lo + i;
       w[i] = __shfl_sync(0xffffffffu, s2 < 32 ? w0 : w1, s2 & 31);   // 0 for s2 >= S
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i)
       if (i >= n_spec && w[i] != 0.f)                                 // uniform across the warp
         a[i] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(i) * kHeadDim);
-    }
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
       if (w[i] != 0.f) {
