@@ -365,7 +365,10 @@ def test_full_size_sampled_against_oracle(name, S, sched):
     got = run_gpu(batch, S or None).float().cpu().numpy().astype(np.float64)
     args = oracle_args(batch)
     B = batch.num_seqs
-    seqs = sorted({0, B - 1, B // 2})
+    # the longest sequence too: in the ragged batches it is the one unit cut into S pieces,
+    # whose rows the reduce merges with a second round of loads
+    longest = int(np.argmax(batch.seq_lens.cpu().numpy()))
+    seqs = sorted({0, B - 1, B // 2, longest})
     rows = oracle.verify_attention_rows(*args, seqs=seqs)
     cu = batch.cu_seqlens_q.cpu().tolist()
     ref = np.concatenate([rows[b] for b in seqs])
