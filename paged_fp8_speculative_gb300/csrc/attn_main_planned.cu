@@ -574,7 +574,8 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
       };
       // The piece's tile sequence is decided by the K producer and handed to every other
       // role through the ring (first page of each tile, then -1).
-      //  - chunks: tiles 0 .. ntiles-1 of the piece (first page pb + 8 j);
+      //  - fixed ranges (deterministic mode): tiles 0 .. ntiles-1 of the piece (first page
+      //    pb + 8 j);
       //  - shared tiles (each CTA holds one piece, all pieces of a unit run together): piece s
       //    of n takes tiles s and s + n of the unit, then tiles 2n + c with c claimed from the
       //    unit's counter, so the unit's CTAs finish within about a tile of each other
@@ -623,7 +624,7 @@ attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
         const int np = min(kPagesPerTile, x.pe - pg0);
         const int st = t % kStages;
         // One page per lane, loads in parallel.  The first tile's address comes from the
-        // cursor alone, so its entries are fetched together with the piece's lengths.
+        // plan alone (not from a claim), so its entries load while the first claims fly.
         const int pg_first = prm.shared_tiles ? x.s * kPagesPerTile : x.vp0;
         const int pg_spec = (j == 0 ? pg_first : pg0) + lane;
         int phys = (lane < kPagesPerTile && pg_spec < p.max_pages) ? bt[pg_spec] : 0;
