@@ -4,27 +4,29 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <atomic>
 
 #include <math.h>
-#include <atomic>
 #include <stddef.h>
 
 namespace mtpattn {
 
 int device_sm_count(int device) {
-  static int cache[64] = {0};
+  // Filled on first use per device; atomics, since calls may come from several host threads.
+  static std::atomic<int> cache[64];
   if (device < 0) {
     if (cudaGetDevice(&device) != cudaSuccess) return -1;
   }
   if (device >= 64) return -1;
-  if (cache[device] > 0) return cache[device];
+  const int cached = cache[device].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       sms <= 0) {
     cudaGetLastError();
     return -1;
   }
-  cache[device] = sms;
+  cache[device].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
