@@ -23,12 +23,18 @@ single key, the probability-underflow spike case including the value printed
 on the aiter PR #7375 page), and invariants (page permutation, decode
 equivalence, descale linearity, causal reach).  tests/test_oracle_mutants.py
 plants plausible mistakes here and checks that the pins catch them.
+
+``oracle.prefill`` is the same kind of definition for the second workload, fp8 varlen
+prefill attention with query/key head dim 192 and value head dim 128 (aiter PR #7375
+page); it is pinned by tests/test_oracle_prefill_pins.py and
+tests/test_oracle_prefill_mutants.py.  The library has no prefill kernel yet.
 """
 from .formats import E4M3_TABLE, e4m3_value, bf16_bits_to_f64, bf16_ulp
 from .attention import (kv_head_of, last_visible_key, gather_keys, verify_attention,
                         verify_attention_rows)
 from .metrics import max_err_over_std, excess_over_half_ulp
+from . import prefill
 
 __all__ = ["E4M3_TABLE", "e4m3_value", "bf16_bits_to_f64", "bf16_ulp", "kv_head_of",
            "last_visible_key", "gather_keys", "verify_attention", "verify_attention_rows",
-           "max_err_over_std", "excess_over_half_ulp"]
+           "max_err_over_std", "excess_over_half_ulp", "prefill"]
