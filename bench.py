@@ -456,8 +456,10 @@ def run_ours(a) -> None:
         "warmup": a.warmup, "ms_per_step": ms / a.steps, "us_per_call": us_call,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic",
-        "config": workload_config(a) | {"num_segments": S, "scheduling": (
-            "planned" if api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED else "chunked")},
+        "config": workload_config(a) | {"num_segments": S},
+        # how this implementation cut the work (not part of the workload, so not in config)
+        "scheduling": ("planned" if api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+                       else "chunked"),
         "frac_of_8tbs_nominal": value / world / 8.0,
         "read_ceiling": {"value_gbs": ceiling_gbs, "frac": value / world * 1e3 / ceiling_gbs,
                          "kernel": "mtpattn_stream_read, 16-B loads"},
