@@ -73,7 +73,9 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     uint8 or float8_e4m3fn codes; block_tables [B, max_pages] int32; seq_lens [B]
     int32; cu_seqlens_q [B+1] int32; descales 1-element float32 device tensors
     (a Python float is copied to the device).  ``status`` is an optional int32
-    device word that collects device-side error bits (ERR_*).
+    device word that collects device-side error bits (ERR_*).  Without ``workspace`` a zeroed
+    one is allocated for this call; a decode loop passes its own (zeroed once, reused by every
+    call on the stream) so that no call allocates.
     """
     if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
         raise ValueError("q must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
