@@ -54,6 +54,8 @@ def parse_args():
                     help="keep warming up at least this long (steady clocks and power)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ceiling-gib", type=float, default=4.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other configurations after the headline one")
     return ap.parse_args()
 
 
@@ -273,6 +275,92 @@ def job_tbs(kv_bytes_per_rank: int, world: int, steps: int, ms: float) -> float:
     return world * kv_bytes_per_rank * steps / (ms * 1e-3) / 1e12
 
 
+# Every configuration of the workload list is also timed in the same run, the same way as
+# the headline one (cold L2 through rotating KV replicas, CUDA events around back-to-back
+# calls after warm-up): name -> (num_segments, 0 = the library's heuristic; KV replicas).
+PER_CONFIG = {
+    "verify_16x35k_gqa16": (16, 8),
+    "verify_16x70k_gqa16": (16, 8),
+    "verify_16x35k_gqa8": (16, 8),
+    "verify_4x35k_gqa16": (64, 8),
+    "draft_extend_8": (0, 16),
+    "decode_8": (0, 16),
+}
+
+
+def alg_bytes_of(batch) -> int:
+    """Algorithmic bytes of one call: K/V, Q and out, and the block-table entries read."""
+    total_pages = sum((int(c) + 15) // 16 for c in batch.seq_lens.tolist())
+    return batch.kv_bytes() + 2 * batch.q.numel() * 2 + 4 * total_pages * batch.num_kv_heads
+
+
+def time_calls(call, R: int, warmup: int, steps: int, warm_seconds: float, stream,
+               barrier=None) -> float:
+    """Milliseconds for `steps` back-to-back calls (CUDA events on the launching stream) after
+    `warmup` calls and at least `warm_seconds` of calls; call(i) uses KV replica i % R.
+    `barrier` (multi-rank runs) is called between the warm-up and the timed region."""
+    import torch
+    t_end = time.time() + warm_seconds
+    i = 0
+    while i < warmup or time.time() < t_end:
+        call(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+        torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        call(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
+def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) -> dict:
+    """us/call, effective TB/s and roofline fraction of every configuration, measured in this
+    process on this GPU (each with its own clock record)."""
+    import torch
+    res = {}
+    for name, (S0, R) in PER_CONFIG.items():
+        if names is not None and name not in names:
+            continue
+        b = synth.workload(name, seed=1, replicas=R, device="cuda")
+        tables = [b.block_tables] + b.replica_tables
+        S = S0 or api.mtp_verify_attn_num_segments(b.num_seqs, b.num_kv_heads,
+                                                   b.block_tables.shape[1])
+        kd = torch.tensor([b.k_descale], dtype=torch.float32, device=dev)
+        vd = torch.tensor([b.v_descale], dtype=torch.float32, device=dev)
+        ws = torch.zeros(api.mtp_verify_attn_workspace_size(b.total_q, b.num_q_heads, S),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(b.q)
+
+        def call(i):
+            api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, tables[i % len(tables)],
+                                    b.seq_lens, b.cu_seqlens_q, kd, vd, b.softmax_scale,
+                                    num_segments=S, out=out, workspace=ws, stream=stream)
+
+        # a short probe sizes the timed region to about a quarter of a second
+        probe = time_calls(call, len(tables), max(3, warmup), 20, 0.0, stream) / 20
+        steps = max(200, int(250.0 / max(probe, 1e-3)))
+        clocks = ClockSampler(uuid)
+        ms = time_calls(call, len(tables), max(3, warmup), steps, 0.3, stream)
+        clk = clocks.stop()
+        us = 1e3 * ms / steps
+        kv = b.kv_bytes()
+        res[name] = {"us_per_call": us, "tbs": kv / (us * 1e-6) / 1e12,
+                     "frac_of_8tbs_nominal": kv / (us * 1e-6) / 8e12,
+                     "roofline_frac": alg_bytes_of(b) / (us * 1e-6) / 1e9 / peak,
+                     "num_segments": S, "kv_replicas": R, "kv_bytes": kv, "steps": steps,
+                     "clocks": clk}
+        del b, tables, ws, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(a) -> None:
     import torch
     import torch.distributed as dist
@@ -310,8 +398,7 @@ def run_ours(a) -> None:
                                 workspace=ws, stream=stream)
 
     kv_bytes = batch.kv_bytes()
-    total_pages = sum((int(c) + 15) // 16 for c in batch.seq_lens.tolist())
-    alg_bytes = kv_bytes + 2 * batch.q.numel() * 2 + 4 * total_pages * batch.num_kv_heads
+    alg_bytes = alg_bytes_of(batch)
 
     # streaming-read ceiling, in the same session
     ceil_buf = torch.empty(int(a.ceiling_gib * (1 << 30)) // 16 * 16, dtype=torch.uint8, device=dev)
@@ -334,30 +421,14 @@ def run_ours(a) -> None:
         pass
     clocks = ClockSampler(uuid)
 
-    # warm-up: W calls, and at least `warm_seconds` of calls
-    t_end = time.time() + a.warm_seconds
-    i = 0
-    while i < a.warmup or time.time() < t_end:
-        call(i)
-        i += 1
-        if i % 64 == 0:
-            torch.cuda.synchronize()
-    torch.cuda.synchronize()
-
-    # timed region
+    # warm-up: W calls and at least `warm_seconds` of calls, a barrier across ranks, then the
+    # timed region (every rank's events bracket its own calls)
+    ms = time_calls(call, R, a.warmup, a.steps, a.warm_seconds, stream,
+                    barrier=dist.barrier if world > 1 else None)
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(a.steps):
-        call(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    ms = t0.elapsed_time(t1)
     clk = clocks.stop()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     # End to end through the public API: every step uploads its inputs from pinned host memory
     # and downloads its output.  Run the way a decode loop runs it, as CUDA graphs captured from
@@ -445,10 +516,15 @@ def run_ours(a) -> None:
         dist.destroy_process_group()
     if rank != 0:
         return
+    peak, peak_kind = hbm_peak()
+    per_config = None
+    if world == 1 and not a.no_per_config:
+        del sets, h_q, h_bt, h_out
+        torch.cuda.empty_cache()
+        per_config = per_config_numbers(api, synth, dev, stream, peak, a.warmup, uuid)
 
     us_call = 1e3 * ms / a.steps
     value = job_tbs(kv_bytes, world, a.steps, ms)
-    peak, peak_kind = hbm_peak()
     achieved = alg_bytes / (us_call * 1e-6) / 1e9
     traffic = ncu_traffic(a.workload)
     line = {
@@ -476,6 +552,8 @@ def run_ours(a) -> None:
                               "steps' compute"},
         "gpu_launches": 2 * a.steps,
         "clocks": clk,
+        # every configuration, each timed like the headline one in this run (not part of value)
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 

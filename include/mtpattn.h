@@ -97,7 +97,8 @@ int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
                                      int32_t max_pages_per_seq, int32_t device);
 
 /*
- * Bytes of device workspace mtp_verify_attn_fwd needs: a 4096-byte header of
+ * Bytes of device workspace mtp_verify_attn_fwd needs (the library's own sizing
+ * rule; the pages print no counterpart): a 4096-byte header of
  * tile counters (one per (sequence, KV head) unit, up to 1024 units), then
  * float32 partial log-sum-exps [total_q * num_q_heads][num_segments], then
  * float32 partial outputs [total_q * num_q_heads][num_segments][256], each region
@@ -123,10 +124,13 @@ size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int3
  *  num_segments in [1, 64], or 0 for mtp_verify_attn_num_segments().
  *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned.
  *               Its first 4096 bytes (the counter header) must be zero before the
- *               workspace's first use (e.g. one cudaMemset); every call, also one that
- *               reports a device error, leaves them zero, so the workspace can be reused
- *               by calls of any shape without clearing.  The rest need not be
- *               initialised.  Calls that overlap on the GPU must use different workspaces.
+ *               workspace's first use (e.g. one cudaMemset); every call that returns
+ *               MTPATTN_OK, also one that reports a device error, leaves them zero, so
+ *               the workspace can be reused by calls of any shape without clearing.
+ *               After MTPATTN_E_LAUNCH the main kernel may have run without the reduce
+ *               that resets them: zero the header again before reusing the workspace.
+ *               The rest need not be initialised.  Calls that overlap on the GPU must
+ *               use different workspaces.
  *  out          device bf16 [total_q][num_q_heads][256]; element strides out_stride_tok,
  *               out_stride_head (multiples of 8), unit stride along head_dim.
  *  status       optional device int32 (NULL = none); device-side MTPATTN_ERR_* bits are
@@ -167,11 +171,16 @@ int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_he
  * Calls needing more scratch than that (mtp_verify_attn_workspace_size() of the
  * resolved segment count) return MTPATTN_E_SCRATCH_LIMIT and launch nothing.
  * The first call on each device looks up the array's device address with that
- * device current, clears it (a synchronous cudaMemset) and caches the address; make
- * that first call before any stream capture.
- * Every call on a device shares the one array, so calls that overlap on the GPU
- * (other streams, other threads) race on it and must be serialised by the caller.  Other return codes and the device
- * status bits are those of mtp_verify_attn_fwd.
+ * device current (cudaGetSymbolAddress), caches it, and clears the array's
+ * 4096-byte counter header with cudaMemsetAsync on `stream`, so the clear is
+ * ordered before the call's kernels on any kind of stream; make that first call
+ * before any stream capture.  After a call that returned MTPATTN_E_LAUNCH (its
+ * reduce may not have run to reset the counters) the next call clears the
+ * header again the same way.
+ * Every call on a device shares the one array and leaves its contents behind,
+ * so calls that overlap on the GPU (other streams, other threads) race on it and
+ * must be serialised by the caller.  Host calls are serialised by a mutex.
+ * Other return codes and the device status bits are those of mtp_verify_attn_fwd.
  */
 int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                                        const void* k_cache, const void* v_cache, int64_t num_pages,
@@ -184,9 +193,13 @@ int mtp_verify_attn_fwd_static_scratch(const void* q, int64_t q_stride_tok, int6
                                        int64_t out_stride_head, int32_t* status, void* stream);
 
 /*
- * Process-wide scheduling switch for later calls: 1 = fixed page ranges per piece
+ * Scheduling switch for later calls: 1 = fixed page ranges per piece
  * (bit-identical results across calls), 0 = balanced tile sharing (the default;
  * see the top of this file).  Thread-safe; takes effect at the next launch.
+ * The switch is PROCESS-WIDE: it changes the results' bit pattern (not their
+ * accuracy) for every caller of the library in the process, on every thread and
+ * device, so a library that needs bit-identical repeats should set it once at
+ * start-up rather than around its own calls.  No counterpart on the pages.
  */
 void mtp_verify_attn_set_deterministic(int32_t on);
 int32_t mtp_verify_attn_get_deterministic(void);
@@ -201,21 +214,24 @@ int32_t mtp_verify_attn_get_deterministic(void);
  *  - MTPATTN_SCHED_CHUNKED: from the host-side shape alone, every unit is cut as
  *    if it held max_pages pages; short sequences leave their SMs idle.
  * Returns MTPATTN_E_ARG for an unknown mode.  Thread-safe; takes effect at the
- * next launch.
+ * next launch.  Like the deterministic switch it is PROCESS-WIDE: it selects the
+ * kernel (and the num_segments heuristic) for every caller in the process.  No
+ * counterpart on the pages, which leave the split of a sequence open.
  */
 #define MTPATTN_SCHED_CHUNKED 0
 #define MTPATTN_SCHED_PLANNED 1
 int32_t mtp_verify_attn_set_scheduling(int32_t mode);
 int32_t mtp_verify_attn_get_scheduling(void);
 
-/* Static description of a status code (never NULL). */
+/* Static description of a status code (never NULL).  The library's own; no counterpart
+ * on the pages. */
 const char* mtp_verify_attn_strerror(int status);
 
 /*
  * Streaming-read ceiling probe (the device's practical read bandwidth, measured
  * the way the aiter PR #5190 page quotes its 5.9-6.9 TB/s ceiling): every byte
  * of the device buffer `buf` (`bytes`, a multiple of 16, 16-byte aligned) is
- * read once with 16-byte loads by `blocks` CTAs (0 = 4 per SM) and folded into
+ * read once with 16-byte loads by `blocks` CTAs (0 = 2 per SM) and folded into
  * one uint32 per CTA written to device `sink` [blocks], so the reads are not
  * dead code.  One kernel launch on `stream`.
  */

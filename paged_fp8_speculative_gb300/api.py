@@ -60,6 +60,35 @@ def _descale(x, device) -> torch.Tensor:
     return torch.full((1,), float(x), dtype=torch.float32, device=device)
 
 
+def _check_args(q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, kd, vd, out):
+    """The shape, dtype and layout checks both entry points share (the C side checks
+    pointers, strides, alignment and the envelope, but cannot see shapes)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
+        raise ValueError("q must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
+    if k_cache.dtype not in (torch.uint8, torch.float8_e4m3fn) or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache / v_cache must be uint8 or float8_e4m3fn codes")
+    if k_cache.dim() != 4 or k_cache.shape[1] != PAGE_SIZE or k_cache.shape[3] != HEAD_DIM:
+        raise ValueError("k_cache must be [num_pages, 16, H_kv, 256]")
+    if v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or not v_cache.is_contiguous():
+        raise ValueError("k_cache and v_cache must be contiguous and of the same shape")
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
+                    ("cu_seqlens_q", cu_seqlens_q)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    num_seqs = seq_lens.numel()
+    if seq_lens.dim() != 1 or block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or \
+            cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() != num_seqs + 1:
+        raise ValueError("block_tables [B, max_pages], seq_lens [B], cu_seqlens_q [B+1]")
+    for name, t in (("k_descale", kd), ("v_descale", vd)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() != 1:
+            raise ValueError(f"{name} must be a 1-element float32 tensor")
+    total_q, hq, _ = q.shape
+    if out is not None and (out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM)
+                            or out.stride(2) != 1):
+        raise ValueError("out must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
+    return num_seqs, total_q, hq, k_cache.shape[2]
+
+
 def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor,
                         cu_seqlens_q: torch.Tensor, k_descale, v_descale,
@@ -77,36 +106,16 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     one is allocated for this call; a decode loop passes its own (zeroed once, reused by every
     call on the stream) so that no call allocates.
     """
-    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
-        raise ValueError("q must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
-    if k_cache.dtype not in (torch.uint8, torch.float8_e4m3fn) or v_cache.dtype != k_cache.dtype:
-        raise ValueError("k_cache / v_cache must be uint8 or float8_e4m3fn codes")
-    if k_cache.dim() != 4 or k_cache.shape[1] != PAGE_SIZE or k_cache.shape[3] != HEAD_DIM:
-        raise ValueError("k_cache must be [num_pages, 16, H_kv, 256]")
-    if v_cache.shape != k_cache.shape or not k_cache.is_contiguous() or not v_cache.is_contiguous():
-        raise ValueError("k_cache and v_cache must be contiguous and of the same shape")
-    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens),
-                    ("cu_seqlens_q", cu_seqlens_q)):
-        if t.dtype != torch.int32 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 tensor")
-    num_seqs = seq_lens.numel()
-    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or cu_seqlens_q.numel() != num_seqs + 1:
-        raise ValueError("block_tables [B, max_pages], seq_lens [B], cu_seqlens_q [B+1]")
-    total_q, hq, _ = q.shape
-    hkv = k_cache.shape[2]
     dev = q.device
     kd = _descale(k_descale, dev)
     vd = _descale(v_descale, dev)
-    for name, t in (("k_descale", kd), ("v_descale", vd)):
-        if t.dtype != torch.float32 or t.numel() != 1:
-            raise ValueError(f"{name} must be a 1-element float32 tensor")
+    num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
+                                             cu_seqlens_q, kd, vd, out)
     if num_segments is None or num_segments == 0:
         num_segments = mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
                                                     dev.index if dev.index is not None else -1)
     if out is None:
         out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    if out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM) or out.stride(2) != 1:
-        raise ValueError("out must be bf16 [total_q, H_q, 256] with unit stride on head_dim")
     need = mtp_verify_attn_workspace_size(total_q, hq, num_segments)
     if workspace is None:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
@@ -136,15 +145,21 @@ def mtp_verify_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor,
 
     The split-KV partials go to the library's own static device array
     (STATIC_SCRATCH_BYTES per GPU), so this wrapper allocates nothing either:
-    ``out``, the descale tensors and every input are the caller's.  Calls that
-    overlap on the GPU share that array and race; serialise them.
+    ``out``, the descale tensors (1-element float32 device tensors, not Python
+    floats) and every input are the caller's, and they get the same checks as in
+    mtp_verify_attn_fwd.  Calls that overlap on the GPU share that array and race;
+    serialise them.
     """
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
+                                             cu_seqlens_q, k_descale, v_descale, out)
     rc = lib().mtp_verify_attn_fwd_static_scratch(
         _ptr(q), q.stride(0), q.stride(1),
         _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
         _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), _ptr(cu_seqlens_q),
-        seq_lens.numel(), q.shape[0], q.shape[1], k_cache.shape[2],
+        num_seqs, total_q, hq, hkv,
         _ptr(k_descale), _ptr(v_descale), float(softmax_scale), int(num_segments),
         _ptr(out), out.stride(0), out.stride(1),
         _ptr(status), _stream_handle(stream))

@@ -14,9 +14,15 @@
 // address, so the address the kernels get comes from cudaGetSymbolAddress,
 // looked up once per device with that device current (on the first call on
 // that device) and cached.  Every call shares the array: calls that overlap on
-// the GPU race on it.  The workspace's counter header must be zero when a call
-// starts: the array is cleared once, on the first call on its device, and every
-// call leaves the header zero again (the partials need no clearing).
+// the GPU race on it.
+//
+// The workspace's counter header (its first kWorkspaceHeaderBytes) must be zero
+// when a call starts; every call that runs both of its kernels leaves it zero
+// again, and the partials behind it need no clearing.  The header is cleared
+// with cudaMemsetAsync on the caller's stream, so the clear is ordered before
+// the call's kernels whatever kind of stream the caller uses: on the first call
+// on each device, and on the next call after one whose reduce could not be
+// launched (E_LAUNCH), which may have left the counters non-zero.
 #include "common.cuh"
 
 #include <mutex>
@@ -28,19 +34,28 @@ static __device__ __align__(256) unsigned char g_static_scratch[MTPATTN_STATIC_S
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+bool g_header_dirty[kMaxDevices] = {false};   // the header must be cleared before the next call
 
-// Device address of the scratch array on the current device (nullptr on failure).
-void* scratch_address(int device) {
+// Device address of the scratch array on `device` (the current device), with its header
+// cleared on `stream` if that is still owed (nullptr on failure).  Called under the mutex.
+void* scratch_address(int device, cudaStream_t stream) {
   if (device < 0 || device >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_addr[device]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr ||
-        cudaMemset(ptr, 0, MTPATTN_STATIC_SCRATCH_BYTES) != cudaSuccess) {   // the entry state
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return nullptr;
     }
     g_scratch_addr[device] = ptr;
+    g_header_dirty[device] = true;          // the entry state: clear once, in stream order
+  }
+  if (g_header_dirty[device]) {
+    if (cudaMemsetAsync(g_scratch_addr[device], 0, mtpattn::kWorkspaceHeaderBytes, stream) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_header_dirty[device] = false;
   }
   return g_scratch_addr[device];
 }
@@ -66,12 +81,18 @@ extern "C" int mtp_verify_attn_fwd_static_scratch(
   }
   const size_t need = mtp_verify_attn_workspace_size(total_q, num_q_heads, num_segments);
   if (need > static_cast<size_t>(MTPATTN_STATIC_SCRATCH_BYTES)) return MTPATTN_E_SCRATCH_LIMIT;
-  void* scratch = scratch_address(device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  void* scratch = scratch_address(device, st);
   if (!scratch) return MTPATTN_E_DEVICE;
-  return mtp_verify_attn_fwd(q, q_stride_tok, q_stride_head, k_cache, v_cache, num_pages,
-                             block_tables, max_pages_per_seq, seq_lens, cu_seqlens_q, num_seqs,
-                             total_q, num_q_heads, num_kv_heads, k_descale, v_descale,
-                             softmax_scale, num_segments, scratch,
-                             static_cast<size_t>(MTPATTN_STATIC_SCRATCH_BYTES), out,
-                             out_stride_tok, out_stride_head, status, stream);
+  const int rc = mtp_verify_attn_fwd(q, q_stride_tok, q_stride_head, k_cache, v_cache, num_pages,
+                                     block_tables, max_pages_per_seq, seq_lens, cu_seqlens_q,
+                                     num_seqs, total_q, num_q_heads, num_kv_heads, k_descale,
+                                     v_descale, softmax_scale, num_segments, scratch,
+                                     static_cast<size_t>(MTPATTN_STATIC_SCRATCH_BYTES), out,
+                                     out_stride_tok, out_stride_head, status, stream);
+  // A failed launch may come after the main kernel ran without the reduce that resets the
+  // tile counters: clear the header again before the next call.
+  if (rc == MTPATTN_E_LAUNCH) g_header_dirty[device] = true;
+  return rc;
 }

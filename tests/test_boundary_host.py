@@ -148,3 +148,28 @@ def test_scheduling_switch():
     finally:
         api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
     assert api.mtp_verify_attn_get_scheduling() == api.SCHED_PLANNED
+
+
+def test_static_wrapper_checks_shapes_before_the_call():
+    """The allocation-free wrapper gets the same shape checks as the workspace wrapper, and
+    takes descales only as tensors (so that it allocates nothing)."""
+    from paged_fp8_speculative_gb300 import synth
+    b = synth.make_batch([40, 20], [4, 2], 16, 1, seed=1)
+    kd = torch.ones(1, dtype=torch.float32)
+    out = torch.empty_like(b.q)
+    f = api.mtp_verify_attn_fwd_static_scratch
+    base = dict(q=b.q, k_cache=b.k_cache, v_cache=b.v_cache, block_tables=b.block_tables,
+                seq_lens=b.seq_lens, cu_seqlens_q=b.cu_seqlens_q, k_descale=kd, v_descale=kd,
+                softmax_scale=0.0625, num_segments=4, out=out)
+    bad = [dict(block_tables=b.block_tables.t()),                 # not contiguous
+           dict(k_cache=b.k_cache[0]),                             # wrong rank
+           dict(v_cache=b.v_cache[:1]),                            # shape differs from K
+           dict(k_descale=1.0),                                    # not a tensor
+           dict(v_descale=torch.ones(2)),                          # not one element
+           dict(out=out[:, :8]),                                   # wrong shape
+           dict(out=None),                                         # it would need allocating
+           dict(q=b.q.float()),                                    # wrong dtype
+           dict(cu_seqlens_q=b.cu_seqlens_q[:-1])]                 # wrong length
+    for over in bad:
+        with pytest.raises(ValueError):
+            f(**(base | over))

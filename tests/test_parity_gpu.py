@@ -361,7 +361,21 @@ def test_num_segments_heuristic_on_device():
 def test_full_size_sampled_against_oracle(name, S, sched):
     """The benchmark shapes at full size, in the launch configuration the bench
     times, checked on sampled sequences the oracle computes one by one."""
-    batch = synth.workload(name, seed=1, device="cuda")
+    _full_size(name, S, "amax")
+
+
+@pytest.mark.parametrize("name,S", [("verify_16x35k_gqa16", 16), ("verify_16x70k_gqa16", 16),
+                                    ("draft_extend_8", 0)])
+def test_full_size_unit_recipe_sampled_against_oracle(name, S, sched):
+    """The same at full size with K/V codes e4m3(x), x ~ N(0, 1): logits of order one, so
+    tens of thousands of comparable weights accumulate in every row.  This exercises the
+    lazy rescaling and the scaled hi/lo encoding of P over 35k-70k keys, which the
+    near-argmax softmax of the per-tensor-amax recipe leaves mostly idle."""
+    _full_size(name, S, "unit")
+
+
+def _full_size(name, S, recipe):
+    batch = synth.workload(name, seed=1, device="cuda", kv_recipe=recipe)
     got = run_gpu(batch, S or None).float().cpu().numpy().astype(np.float64)
     args = oracle_args(batch)
     B = batch.num_seqs

@@ -6,13 +6,22 @@ synchronise the device), so this entry point keeps its split-KV partials in a
 library-owned static device array.  The test calls it through the C ABI twice in
 a row, on different batches, and checks each output against the regular entry
 point (which uses a caller workspace): bit for bit, under deterministic
-scheduling.  It also checks that a call too large for the array is refused.
+scheduling.  It also checks that a call too large for the array is refused;
+that the first call of a fresh process, made on a non-default stream under
+balanced scheduling, matches the oracle (the one-time clear of the array's
+counter header is ordered on the caller's stream); and that a call which sets a
+device error bit leaves the shared header zero, so the next call still matches
+the workspace entry point bit for bit.
 This file is collected last so a stop-at-first-failure run has run every other
 test before it; it passes alone in a fresh process as well.
 """
 from __future__ import annotations
 
 import ctypes
+import os
+import subprocess
+import sys
+import textwrap
 
 import numpy as np
 import pytest
@@ -88,3 +97,73 @@ def test_static_scratch_refuses_calls_beyond_its_size():
     assert _c_call(b, kd, kd, 16, out, status) == api.OK
     torch.cuda.synchronize()
     assert status.item() == 0
+
+
+def test_static_scratch_after_a_device_error_is_bit_identical():
+    """A call whose block table names a page outside the pool sets ERR_PAGE; the shared
+    array's tile counters must still be back at zero afterwards, so the next (valid) call
+    equals the workspace entry point bit for bit under deterministic scheduling."""
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        b = synth.make_batch([2500, 700, 40], [4, 3, 1], 16, 1, seed=904, k_descale=0.5,
+                             v_descale=2.0).to("cuda")
+        kd = torch.tensor([b.k_descale], dtype=torch.float32, device="cuda")
+        vd = torch.tensor([b.v_descale], dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bad_bt = b.block_tables.clone()
+        bad_bt[0, 5] = b.k_cache.shape[0] + 3
+        bad = synth.PagedBatch(b.q, b.k_cache, b.v_cache, bad_bt, b.seq_lens, b.cu_seqlens_q,
+                               b.k_descale, b.v_descale, b.softmax_scale, 1, 16)
+        out = torch.empty_like(b.q)
+        assert _c_call(bad, kd, vd, 8, out, status) == api.OK
+        torch.cuda.synchronize()
+        assert status.item() & api.ERR_PAGE
+        assert out[:4].abs().max().item() == 0          # the bad sequence's rows are zeros
+        status.zero_()
+        ref = _regular(b, kd, vd, 8)
+        out2 = torch.full_like(b.q, float("nan"))
+        assert _c_call(b, kd, vd, 8, out2, status) == api.OK
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert torch.equal(out2, ref)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
+_FRESH = textwrap.dedent("""
+    import sys
+    import numpy as np
+    import torch
+    sys.path.insert(0, {root!r})
+    import oracle
+    from paged_fp8_speculative_gb300 import api, synth
+    from tests.helpers import oracle_args
+    assert not api.mtp_verify_attn_get_deterministic()      # balanced tile sharing
+    batch = synth.make_batch([6000, 3000, 900], [4, 2, 3], 16, 1, seed=905, k_descale=0.5,
+                             v_descale=2.0)
+    side = torch.cuda.Stream()                              # a non-default stream
+    with torch.cuda.stream(side):
+        gb = batch.to("cuda")
+        kd = torch.tensor([gb.k_descale], dtype=torch.float32, device="cuda")
+        vd = torch.tensor([gb.v_descale], dtype=torch.float32, device="cuda")
+        out = torch.empty_like(gb.q)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        api.mtp_verify_attn_fwd_static_scratch(gb.q, gb.k_cache, gb.v_cache, gb.block_tables,
+                                               gb.seq_lens, gb.cu_seqlens_q, kd, vd,
+                                               gb.softmax_scale, 16, out, status=status,
+                                               stream=side)
+    side.synchronize()
+    ref = oracle.verify_attention(*oracle_args(batch))
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = oracle.excess_over_half_ulp(got, ref)
+    assert status.item() == 0, status.item()
+    assert np.isfinite(got).all() and err <= {tol}, err
+    print("fresh-process static call ok", err)
+""")
+
+
+def test_static_scratch_first_call_on_a_side_stream_in_a_fresh_process():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH.format(root=root, tol=TOL)], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
