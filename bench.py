@@ -330,6 +330,7 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
             continue
         b = synth.workload(name, seed=1, replicas=R, device="cuda")
         tables = [b.block_tables] + b.replica_tables
+        # S0 = 0: the library chooses S at every call (and may share the slots out by length)
         S = S0 or api.mtp_verify_attn_num_segments(b.num_seqs, b.num_kv_heads,
                                                    b.block_tables.shape[1])
         kd = torch.tensor([b.k_descale], dtype=torch.float32, device=dev)
@@ -341,7 +342,7 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
         def call(i):
             api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, tables[i % len(tables)],
                                     b.seq_lens, b.cu_seqlens_q, kd, vd, b.softmax_scale,
-                                    num_segments=S, out=out, workspace=ws, stream=stream)
+                                    num_segments=S0, out=out, workspace=ws, stream=stream)
 
         # a short probe sizes the timed region to about a quarter of a second
         probe = time_calls(call, len(tables), max(3, warmup), 20, 0.0, stream) / 20

@@ -22,8 +22,8 @@
  * LSE into the bf16 output (aiter PR #5190 page, Modifications: the split-KV
  * main kernel and its segment reduce).  num_segments (S) is the number of split
  * slots per (sequence, KV head): the pages of all units are shared out in equal
- * chunks over the SMs, no unit is cut into more than S pieces, and slots a unit
- * does not use are written empty.  Any S in [1, 64] gives the same result up to
+ * chunks over the SMs, no unit is cut into more than S pieces (unless S was left to
+ * the library, see num_segments below), and slots a unit does not use are written empty.  Any S in [1, 64] gives the same result up to
  * float32 re-association; S = 1 keeps every unit whole.
  *
  * Balanced scheduling (the default): when every unit is cut into whole pieces
@@ -121,7 +121,11 @@ size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int3
  *  k_descale,   device float32, one element each (per-tensor descales).
  *  v_descale
  *  softmax_scale  host float, multiplies the logits (usually 1/sqrt(256)).
- *  num_segments in [1, 64], or 0 for mtp_verify_attn_num_segments().
+ *  num_segments in [1, 64], or 0 for mtp_verify_attn_num_segments().  With 0 (and S >= 3,
+ *               planned scheduling) the workspace's total_q * num_q_heads * S partial slots
+ *               are shared out by length: a long sequence may take more than S pieces (at
+ *               most one per SM) when short ones use fewer.  A ragged batch with one long
+ *               sequence then streams it on every SM instead of on S of them.
  *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned.
  *               Its first 4096 bytes (the counter header) must be zero before the
  *               workspace's first use (e.g. one cudaMemset); every call that returns

@@ -45,6 +45,16 @@ SIGNATURES = {
 _LIB = None
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of the library at ``path`` with the C signatures attached."""
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib() -> ctypes.CDLL:
     """The loaded library (raises RuntimeError if it has not been built)."""
     global _LIB
@@ -52,10 +62,5 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m paged_fp8_speculative_gb300.build`")
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _LIB = handle
+        _LIB = load(LIB_PATH)
     return _LIB

@@ -101,7 +101,9 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     q [total_q, H_q, 256] bf16; k_cache / v_cache [num_pages, 16, H_kv, 256]
     uint8 or float8_e4m3fn codes; block_tables [B, max_pages] int32; seq_lens [B]
     int32; cu_seqlens_q [B+1] int32; descales 1-element float32 device tensors
-    (a Python float is copied to the device).  ``status`` is an optional int32
+    (a Python float is copied to the device).  ``num_segments`` None or 0 lets the library
+    choose S; a long sequence may then take more than S pieces when short ones use fewer
+    (the workspace's rows x S partial slots are shared out by length).  ``status`` is an optional int32
     device word that collects device-side error bits (ERR_*).  Without ``workspace`` a zeroed
     one is allocated for this call; a decode loop passes its own (zeroed once, reused by every
     call on the stream) so that no call allocates.
@@ -111,12 +113,14 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     vd = _descale(v_descale, dev)
     num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
                                              cu_seqlens_q, kd, vd, out)
-    if num_segments is None or num_segments == 0:
-        num_segments = mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
-                                                    dev.index if dev.index is not None else -1)
+    # None / 0: the library chooses S (and may then share the partial slots out by length);
+    # the workspace is sized for the S it will choose.
+    chosen = int(num_segments or 0)
+    S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
+                                               dev.index if dev.index is not None else -1)
     if out is None:
         out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    need = mtp_verify_attn_workspace_size(total_q, hq, num_segments)
+    need = mtp_verify_attn_workspace_size(total_q, hq, S)
     if workspace is None:
         workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     rc = lib().mtp_verify_attn_fwd(
@@ -125,7 +129,7 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
         _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), _ptr(cu_seqlens_q),
         num_seqs, total_q, hq, hkv,
-        _ptr(kd), _ptr(vd), float(softmax_scale), int(num_segments),
+        _ptr(kd), _ptr(vd), float(softmax_scale), chosen,
         _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), out.stride(0), out.stride(1),
         _ptr(status), _stream_handle(stream))

@@ -30,14 +30,19 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libmtpattn.so")
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), lib_path: str = LIB) -> str:
+    """Compile every csrc/*.cu and link ``lib_path``.  ``extra_flags`` (e.g. the test-only
+    -DMTPATTN_WAIT_CYCLES / -DMTPATTN_TEST_STALL of the wait-limit test) go to every nvcc;
+    such builds use their own object folder and library path."""
+    obj_dir = BUILD if lib_path == LIB else os.path.join(BUILD, os.path.splitext(
+        os.path.basename(lib_path))[0])
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     cc = nvcc()
     procs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
@@ -52,13 +57,13 @@ def build(verbose: bool = False, extra_flags=()) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

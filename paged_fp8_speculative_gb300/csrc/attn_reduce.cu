@@ -11,6 +11,11 @@
 // it may start while the main kernel drains and waits (griddepcontrol) until the
 // main kernel's results are visible.
 //
+// Slot pool: when the main kernel laid the partials out unit by unit (AttnParams), a row's
+// first LSE slot holds kPoolMarker and the row's first row-slot and piece count; the row's
+// warps then load its pool LSEs and walk its slots in blocks of 16 (warp g takes blocks
+// g, g + groups, ...).
+//
 // Work split: the S slots of a row form ceil(S / 16) groups of 16, and each
 // (group, half of the row's 256 dims) pair is one warp, 4 dims per lane.  Every
 // warp reads all S LSEs (two per lane: the same few cache lines), so each knows M
@@ -71,7 +76,66 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  if (!bad && mx != -INFINITY) {
+  // Slot pool (see AttnParams): the row's first LSE slot redirects to its partials.  The
+  // loads above were speculative; the row costs one more round trip.
+  // Only this call's layout counts: a marker is honoured only if the call allowed the pool
+  // and its redirect lies inside this call's pool (else the row is treated as an error).
+  const bool pooled = live && p.slot_pool &&
+                      __shfl_sync(0xffffffffu, __float_as_uint(l0), 0) == kPoolMarker;
+  const int off = pooled ? __shfl_sync(0xffffffffu, __float_as_int(l0), 1) : 0;
+  const int P = pooled ? __shfl_sync(0xffffffffu, __float_as_int(l0), 2) : 0;
+  if (pooled && (off < 0 || P < 1 || P > 256 || off > p.pool_cap - P)) {
+    bad = 1;
+  } else if (pooled) {
+    const float* pl = p.pool_lse + off;
+    float lv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) lv[k] = lane + 32 * k < P ? pl[lane + 32 * k] : -INFINITY;
+    bad = 0;
+    mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      bad |= isnan(lv[k]);
+      mx = fmaxf(mx, lv[k]);
+    }
+#pragma unroll
+    for (int off2 = 16; off2 > 0; off2 >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off2));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, off2);
+    }
+    if (!bad && mx != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        lv[k] = lv[k] == -INFINITY ? 0.f : exp2f(lv[k] - mx);    // now the weights
+        wsum += lv[k];
+      }
+#pragma unroll
+      for (int off2 = 16; off2 > 0; off2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off2);
+      // This warp's blocks of 16 slots: g, g + groups, ... (all 16 inside one lane group of 32).
+      const float* ob = p.o_part + static_cast<int64_t>(off) * kHeadDim + part * 128 + lane * 4;
+      for (int s0 = g * kGroup; s0 < P; s0 += groups * kGroup) {
+        const int kk = s0 >> 5;
+        float src = lv[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k)
+          if (k == kk) src = lv[k];
+        float w[kGroup];
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) w[i] = __shfl_sync(0xffffffffu, src, (s0 & 31) + i);
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i)
+          if (s0 + i < P && w[i] != 0.f)
+            a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s0 + i) * kHeadDim);
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+          if (s0 + i < P && w[i] != 0.f) {
+            acc.x = fmaf(w[i], a[i].x, acc.x); acc.y = fmaf(w[i], a[i].y, acc.y);
+            acc.z = fmaf(w[i], a[i].z, acc.z); acc.w = fmaf(w[i], a[i].w, acc.w);
+          }
+        }
+      }
+    }
+  } else if (!bad && mx != -INFINITY) {
     const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
     const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
     wsum = w0 + w1;

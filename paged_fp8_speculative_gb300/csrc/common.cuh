@@ -38,6 +38,15 @@ struct AttnParams {
   int32_t scheduling;    // 0: chunks sized for max_pages, 1: pieces planned from the lengths
   float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
   float* lse_part;      // [total_q * H_q][S] float32, log2-sum-exp2 of the segment (NaN = error)
+  // Slot pool (planned scheduling, when the caller left num_segments to the library): the
+  // plan may give a long unit more than S pieces when short units use fewer.  The o_part
+  // region then holds every unit's partials unit by unit, [row of the unit][piece], pool_cap
+  // row-slots of 256 floats, followed by their LSEs (pool_lse, pool_cap floats); each output
+  // row's first LSE slot holds kPoolMarker, the next two the row's first row-slot and its
+  // number of pieces (as int32 bits).
+  int32_t slot_pool;    // 1: the plan may use the pool layout
+  int32_t pool_cap;     // row-slots of the pool: floor(rows * S * 256 / 257)
+  float* pool_lse;      // o_part + pool_cap * 256
   __nv_bfloat16* out;
   int64_t out_stride_tok, out_stride_head;
   int32_t* status;      // optional
@@ -54,6 +63,10 @@ __host__ __device__ inline void segment_pages(int n_pages, int S, int s, int* be
   *begin = b;
   *end = e;
 }
+
+// LSE bit pattern that marks an output row whose partials are in the slot pool (a NaN no
+// arithmetic produces; the error NaN the kernels write is 0x7fc00000).
+constexpr uint32_t kPoolMarker = 0x7fd00d1eu;
 
 __device__ inline void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);

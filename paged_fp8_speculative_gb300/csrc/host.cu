@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 
 #include <math.h>
 #include <stddef.h>
@@ -129,6 +130,7 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   if (num_segments < 0 || num_segments > MTPATTN_MAX_SEGMENTS) return MTPATTN_E_UNSUPPORTED;
   // 3. the segment count (the heuristic needs the device) and the workspace
   int device = -1;
+  const bool library_chose_s = num_segments == 0;
   if (num_segments == 0) {
     if (cudaGetDevice(&device) != cudaSuccess) {
       cudaGetLastError();
@@ -173,10 +175,18 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   p.num_segments = num_segments;
   p.slots_used = num_segments;
   const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
+  // The slot pool (planned scheduling only): when the library chose S, a long unit may take
+  // more than S pieces if short units use fewer, inside the same rows x S partial slots.
+  p.slot_pool = (library_chose_s && num_segments >= 3) ? 1 : 0;
+  {
+    const int64_t cap = static_cast<int64_t>(rows) * num_segments * kHeadDim / (kHeadDim + 1);
+    p.pool_cap = static_cast<int32_t>(std::min<int64_t>(cap, INT32_MAX / kHeadDim));
+  }
   p.tile_ctr = static_cast<uint32_t*>(workspace);
   p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes);
   p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes +
                                       align_up(rows * num_segments * sizeof(float)));
+  p.pool_lse = p.o_part + static_cast<int64_t>(p.pool_cap) * kHeadDim;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;

@@ -46,7 +46,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // seconds) without progress, or as soon as another role has raised `abort`,
 // the wait gives up and returns false.  The caller then winds down without
 // touching the pipeline again.
+#ifdef MTPATTN_WAIT_CYCLES
+constexpr long long kWaitCycles = MTPATTN_WAIT_CYCLES;   // test builds: a short limit
+#else
 constexpr long long kWaitCycles = 4000000000LL;
+#endif
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -102,6 +106,22 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
       "l"(policy)
       : "memory");
+}
+
+// L2 prefetch of `bytes` contiguous global bytes (16-byte aligned, a multiple of 16); nothing
+// tracks its completion, it only warms L2 for a later copy.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+// L2 prefetch of one box of a 4-D tensor map (out-of-range coordinates fetch nothing).
+__device__ __forceinline__ void prefetch_l2_tile_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                    int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------

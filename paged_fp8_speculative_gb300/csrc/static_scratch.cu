@@ -75,11 +75,14 @@ extern "C" int mtp_verify_attn_fwd_static_scratch(
     cudaGetLastError();
     return MTPATTN_E_DEVICE;
   }
+  // 0 stays 0 in the call below (the library then chooses S, and may share the slots out by
+  // length); the size check uses the S it will choose.
+  int32_t s_resolved = num_segments;
   if (num_segments == 0 && num_seqs > 0 && num_kv_heads > 0 && max_pages_per_seq > 0) {
-    num_segments = mtp_verify_attn_num_segments(num_seqs, num_kv_heads, max_pages_per_seq, device);
-    if (num_segments < 1) return MTPATTN_E_DEVICE;
+    s_resolved = mtp_verify_attn_num_segments(num_seqs, num_kv_heads, max_pages_per_seq, device);
+    if (s_resolved < 1) return MTPATTN_E_DEVICE;
   }
-  const size_t need = mtp_verify_attn_workspace_size(total_q, num_q_heads, num_segments);
+  const size_t need = mtp_verify_attn_workspace_size(total_q, num_q_heads, s_resolved);
   if (need > static_cast<size_t>(MTPATTN_STATIC_SCRATCH_BYTES)) return MTPATTN_E_SCRATCH_LIMIT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);

@@ -388,3 +388,97 @@ def _full_size(name, S, recipe):
     ref = np.concatenate([rows[b] for b in seqs])
     res = np.concatenate([got[cu[b]:cu[b + 1]] for b in seqs])
     assert oracle.excess_over_half_ulp(res, ref) <= TOL
+
+
+POOL_MARKER = 0x7fd00d1e
+
+
+def _pool_rows(ws, batch, S):
+    """Output rows whose first split slot carries the slot-pool redirect."""
+    rows = batch.total_q * batch.num_q_heads
+    lse = ws[4096:4096 + rows * S * 4].view(torch.int32).view(rows, S).cpu()
+    return (lse[:, 0] == POOL_MARKER).nonzero().flatten().tolist()
+
+
+@pytest.mark.parametrize("det", [False, True], ids=["balanced", "deterministic"])
+@pytest.mark.parametrize("ctx,ql,hq,hkv", [
+    ([20000, 30, 500, 7], [4, 1, 2, 3], 16, 1),
+    ([9, 41000, 64, 300, 15, 2], [1, 4, 4, 2, 1, 1], 16, 1),
+    ([12000, 100, 2], [3, 4, 1], 16, 2),
+    ([30000, 17, 200], [1, 1, 1], 8, 1),          # decode, GQA 8
+])
+def test_slot_pool_long_unit_takes_more_than_s_pieces(ctx, ql, hq, hkv, det):
+    """When the library chooses S, one long sequence among short ones may take more than S
+    pieces (the workspace's rows x S partial slots are shared out by length).  The output
+    matches the oracle, and the workspace shows that the pool layout was used."""
+    api.mtp_verify_attn_set_deterministic(det)
+    try:
+        batch = synth.make_batch(ctx, ql, hq, hkv, seed=sum(ctx) % 997, kv_recipe="unit",
+                                 k_descale=0.5, v_descale=2.0)
+        gb = batch.to("cuda")
+        S = api.mtp_verify_attn_num_segments(gb.num_seqs, hkv, gb.block_tables.shape[1])
+        kd = torch.tensor([gb.k_descale], device="cuda")
+        vd = torch.tensor([gb.v_descale], device="cuda")
+        ws = torch.zeros(api.mtp_verify_attn_workspace_size(gb.total_q, hq, S), dtype=torch.uint8,
+                         device="cuda")
+        out = api.mtp_verify_attn_fwd(gb.q, gb.k_cache, gb.v_cache, gb.block_tables, gb.seq_lens,
+                                      gb.cu_seqlens_q, kd, vd, gb.softmax_scale, num_segments=0,
+                                      workspace=ws)
+        torch.cuda.synchronize()
+        ref = oracle.verify_attention(*oracle_args(batch))
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert oracle.excess_over_half_ulp(got, ref) <= TOL
+        assert len(_pool_rows(ws, gb, S)) == gb.total_q * hq        # every row redirected
+        assert ws[:4096].count_nonzero().item() == 0                  # counters reset
+        # with an explicit S the same batch keeps the row-major slots and the same result
+        ws.zero_()
+        out2 = api.mtp_verify_attn_fwd(gb.q, gb.k_cache, gb.v_cache, gb.block_tables,
+                                       gb.seq_lens, gb.cu_seqlens_q, kd, vd, gb.softmax_scale,
+                                       num_segments=S, workspace=ws)
+        torch.cuda.synchronize()
+        assert _pool_rows(ws, gb, S) == []
+        got2 = out2.float().cpu().numpy().astype(np.float64)
+        assert oracle.excess_over_half_ulp(got2, ref) <= TOL
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
+def test_slot_pool_device_errors_zero_rows():
+    """A bad page in the long unit under the pool layout: its rows are zeros, ERR_PAGE is set,
+    the other sequences' rows are unaffected (bit for bit, fixed page ranges)."""
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        batch = synth.make_batch([15000, 40, 300], [4, 2, 1], 16, 1, seed=77).to("cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        good = run_gpu(batch, None, status=status)
+        assert status.item() == 0
+        bt = batch.block_tables.clone()
+        bt[0, 700] = -5
+        bad = run_gpu(batch, None, status=status, block_tables=bt)
+        assert status.item() & api.ERR_PAGE
+        assert bad[:4].abs().max().item() == 0
+        assert torch.equal(bad[4:], good[4:])
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+
+
+def test_slot_pool_then_row_major_in_one_workspace():
+    """Calls of both layouts alternate on one workspace without clearing it: a redirect left
+    by a pool call is never followed by a call that uses the row-major slots."""
+    a = synth.make_batch([20000, 30, 500, 7], [4, 1, 2, 3], 16, 1, seed=78)
+    b = synth.make_batch([3000] * 4, [4, 1, 2, 3], 16, 1, seed=79)
+    ga, gbb = a.to("cuda"), b.to("cuda")
+    kd = torch.ones(1, device="cuda")
+    S = max(api.mtp_verify_attn_num_segments(4, 1, ga.block_tables.shape[1]),
+            api.mtp_verify_attn_num_segments(4, 1, gbb.block_tables.shape[1]))
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(ga.total_q, 16, S), dtype=torch.uint8,
+                     device="cuda")
+    refs = {id(a): oracle.verify_attention(*oracle_args(a)),
+            id(b): oracle.verify_attention(*oracle_args(b))}
+    for host, dev, s in ((a, ga, 0), (b, gbb, 4), (a, ga, 0), (b, gbb, 0)):
+        o = api.mtp_verify_attn_fwd(dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
+                                    dev.seq_lens, dev.cu_seqlens_q, kd, kd, dev.softmax_scale,
+                                    num_segments=s, workspace=ws)
+        torch.cuda.synchronize()
+        got = o.float().cpu().numpy().astype(np.float64)
+        assert oracle.excess_over_half_ulp(got, refs[id(host)]) <= TOL

@@ -1,0 +1,78 @@
+"""The main kernel's bounded pipeline waits, exercised without faulting the GPU.
+
+A test-only build of the library (-DMTPATTN_WAIT_CYCLES=200000, about 0.1 ms of SM clocks,
+and -DMTPATTN_TEST_STALL, which makes CTA 0's V producer skip its first tile) is called on a
+small batch: the MMA warp's wait for that tile runs out, the CTA raises its abort flag, every
+role winds down (waiting, again with a limit, for its own copies in flight), the tensor memory
+is freed and the call reports MTPATTN_ERR_TIMEOUT in its status word.  The test then checks
+that the GPU is still usable: a second call of the test build returns the same way, and the
+product library, on the same workspace, matches the oracle.  It runs in a child process so
+that the test build's kernels stay out of the other tests' process.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+_CHILD = textwrap.dedent("""
+    import sys
+    import numpy as np
+    import torch
+    sys.path.insert(0, {root!r})
+    import oracle
+    from paged_fp8_speculative_gb300 import _lib, api, synth
+    from tests.helpers import oracle_args
+
+    stall = _lib.load({path!r})
+    batch = synth.make_batch([3000] * 4, 4, 16, 1, seed=31, k_descale=0.5, v_descale=2.0)
+    b = batch.to("cuda")
+    kd = torch.tensor([b.k_descale], dtype=torch.float32, device="cuda")
+    vd = torch.tensor([b.v_descale], dtype=torch.float32, device="cuda")
+    S = 8
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(b.total_q, 16, S), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.zeros_like(b.q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        status.zero_()
+        rc = stall.mtp_verify_attn_fwd(
+            b.q.data_ptr(), b.q.stride(0), b.q.stride(1), b.k_cache.data_ptr(),
+            b.v_cache.data_ptr(), b.k_cache.shape[0], b.block_tables.data_ptr(),
+            b.block_tables.shape[1], b.seq_lens.data_ptr(), b.cu_seqlens_q.data_ptr(),
+            b.num_seqs, b.total_q, 16, 1, kd.data_ptr(), vd.data_ptr(), b.softmax_scale, S,
+            ws.data_ptr(), ws.numel(), out.data_ptr(), out.stride(0), out.stride(1),
+            status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, rc
+        torch.cuda.synchronize()                      # the call returned
+        assert status.item() & api.ERR_TIMEOUT, status.item()
+        assert ws[:4096].count_nonzero().item() == 0  # the reduce still reset the counters
+    # the product library on the same workspace, with its normal wait limit
+    status.zero_()
+    got = api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                  b.cu_seqlens_q, kd, vd, b.softmax_scale, num_segments=S,
+                                  workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0, status.item()
+    ref = oracle.verify_attention(*oracle_args(batch))
+    err = oracle.excess_over_half_ulp(got.float().cpu().numpy().astype(np.float64), ref)
+    assert err <= 0.01, err
+    print("wait-limit test ok", err)
+""")
+
+
+def test_pipeline_wait_limit_returns_timeout_status():
+    from paged_fp8_speculative_gb300 import build
+    path = os.path.join(build.BUILD, "libmtpattn_stall.so")
+    build.build(extra_flags=("-DMTPATTN_WAIT_CYCLES=200000", "-DMTPATTN_TEST_STALL=1"),
+                lib_path=path)
+    r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT, path=path)], cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
