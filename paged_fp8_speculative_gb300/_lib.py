@@ -1,4 +1,5 @@
-"""ctypes loader for libmtpattn.so (the C ABI declared in include/mtpattn.h).
+"""ctypes loader for libmtpattn.so (the C ABI declared in include/mtpattn.h and
+include/fmha_fp8_varlen.h).
 
 There is no fallback: if the library is missing the import of this module's
 ``lib()`` raises, so no caller can silently run anything else.
@@ -15,7 +16,7 @@ _c_int, _c_i32, _c_i64, _c_size, _c_float = (ctypes.c_int, ctypes.c_int32, ctype
                                              ctypes.c_size_t, ctypes.c_float)
 _vp = ctypes.c_void_p
 
-# name -> (restype, argtypes), in the order of include/mtpattn.h
+# name -> (restype, argtypes), in the order of include/mtpattn.h, then include/fmha_fp8_varlen.h
 SIGNATURES = {
     "mtp_verify_attn_num_segments": (_c_i32, [_c_i32, _c_i32, _c_i32, _c_i32]),
     "mtp_verify_attn_workspace_size": (_c_size, [_c_i32, _c_i32, _c_i32]),
@@ -40,6 +41,19 @@ SIGNATURES = {
     "mtp_verify_attn_strerror": (ctypes.c_char_p, [_c_int]),
     "mtpattn_stream_read": (_c_int, [_vp, _c_size, _vp, _c_i32, _vp]),
     "mtpattn_stream_read_default_blocks": (_c_i32, []),
+    # include/fmha_fp8_varlen.h
+    "fmha_fwd_fp8_varlen": (_c_int, [
+        _vp, _c_i64, _c_i64,            # q, strides (bytes)
+        _vp, _c_i64, _c_i64,            # k, strides
+        _vp, _c_i64, _c_i64,            # v, strides
+        _vp, _vp,                       # cu_seqlens_q, cu_seqlens_k
+        _c_i32, _c_i32, _c_i32,         # num_seqs, total_q, total_k
+        _c_i32, _c_i32,                 # max_seqlen_q, max_seqlen_k
+        _c_i32, _c_i32,                 # num_q_heads, num_kv_heads
+        _vp, _vp, _vp,                  # q/k/v descales
+        _c_float, _c_i32,               # softmax_scale, causal
+        _vp, _c_i64, _c_i64,            # out, strides (elements)
+        _vp, _vp, _vp]),                # lse, status, stream
 }
 
 _LIB = None

@@ -6,6 +6,7 @@ the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import math
 from typing import Optional
 
 import torch
@@ -210,3 +211,65 @@ def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, 
     if rc != OK:
         raise MtpAttnError(rc)
     return sink
+
+
+# ---- fp8 varlen prefill (include/fmha_fp8_varlen.h) ---------------------------------------------
+
+HEAD_DIM_QK = 192
+HEAD_DIM_V = 128
+ERR_CU = 32
+
+
+def fmha_fwd_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_descale, k_descale,
+                        v_descale, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                        max_seqlen_q: int, max_seqlen_k: int, softmax_scale: Optional[float] = None,
+                        is_causal: bool = False, return_lse: bool = False,
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None):
+    """fp8 varlen prefill attention (q/k head dim 192, v 128); returns out, or (out, lse).
+
+    q [total_q, H_q, 192], k [total_k, H_kv, 192], v [total_k, H_kv, 128]: uint8 or
+    float8_e4m3fn codes with unit stride on the head dim; cu_seqlens_q / cu_seqlens_k int32
+    [B+1]; descales 1-element float32 device tensors (a Python float is copied to the
+    device); softmax_scale defaults to 1/sqrt(192); out bf16 [total_q, H_q, 128]; lse float32
+    [H_q, total_q] (natural log), allocated when return_lse and not given.
+    """
+    for name, t, d in (("q", q, HEAD_DIM_QK), ("k", k, HEAD_DIM_QK), ("v", v, HEAD_DIM_V)):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 3 or t.shape[2] != d \
+                or t.stride(2) != 1:
+            raise ValueError(f"{name} must be e4m3 codes [rows, heads, {d}] with unit stride on "
+                             "the head dim")
+    if k.shape[:2] != v.shape[:2]:
+        raise ValueError("k and v must have the same rows and heads")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.dim() != 1:
+            raise ValueError(f"{name} must be a contiguous int32 vector")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have num_seqs + 1 entries")
+    dev = q.device
+    qd, kd, vd = (_descale(x, dev) for x in (q_descale, k_descale, v_descale))
+    for name, t in (("q_descale", qd), ("k_descale", kd), ("v_descale", vd)):
+        if t.dtype != torch.float32 or t.numel() != 1:
+            raise ValueError(f"{name} must be a 1-element float32 tensor")
+    total_q, hq, _ = q.shape
+    total_k, hkv, _ = k.shape
+    if out is None:
+        out = torch.empty(total_q, hq, HEAD_DIM_V, dtype=torch.bfloat16, device=dev)
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM_V) or \
+            out.stride(2) != 1:
+        raise ValueError("out must be bf16 [total_q, H_q, 128] with unit stride on the head dim")
+    if return_lse and lse is None:
+        lse = torch.empty(hq, total_q, dtype=torch.float32, device=dev)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (hq, total_q) or
+                            not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [H_q, total_q] tensor")
+    scale = 1.0 / math.sqrt(HEAD_DIM_QK) if softmax_scale is None else float(softmax_scale)
+    rc = lib().fmha_fwd_fp8_varlen(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        cu_seqlens_q.numel() - 1, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
+        _ptr(qd), _ptr(kd), _ptr(vd), scale, 1 if is_causal else 0,
+        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(status), _stream_handle(stream))
+    if rc != OK:
+        raise MtpAttnError(rc)
+    return (out, lse) if return_lse else out

@@ -197,3 +197,83 @@ def workload(name: str, *, seed: int = 0, replicas: int = 1, device: str = "cpu"
 
 WORKLOADS = ("verify_tiny", "verify_16x35k_gqa16", "verify_16x70k_gqa16", "verify_2x777_kv2",
              "verify_16x35k_gqa8", "verify_4x35k_gqa16", "draft_extend_8", "decode_8")
+
+
+# ---- fp8 varlen prefill inputs (aiter PR #7375 page) ---------------------------------------------
+
+@dataclass
+class PrefillBatch:
+    q: torch.Tensor             # uint8 e4m3 codes [total_q, H_q, 192]
+    k: torch.Tensor             # uint8 e4m3 codes [total_k, H_kv, 192]
+    v: torch.Tensor             # uint8 e4m3 codes [total_k, H_kv, 128]
+    cu_seqlens_q: torch.Tensor  # int32 [B + 1]
+    cu_seqlens_k: torch.Tensor  # int32 [B + 1]
+    q_descale: float
+    k_descale: float
+    v_descale: float
+    max_seqlen_q: int
+    max_seqlen_k: int
+
+    def to(self, device) -> "PrefillBatch":
+        mv = lambda t: t.to(device)
+        return PrefillBatch(mv(self.q), mv(self.k), mv(self.v), mv(self.cu_seqlens_q),
+                            mv(self.cu_seqlens_k), self.q_descale, self.k_descale, self.v_descale,
+                            self.max_seqlen_q, self.max_seqlen_k)
+
+    def flops(self, causal: bool) -> int:
+        """Both products over the visible (query, key) pairs: 2 * (192 + 128) per pair and
+        query head (the page's TFLOPS count)."""
+        hq = int(self.q.shape[1])
+        cq = self.cu_seqlens_q.tolist()
+        ck = self.cu_seqlens_k.tolist()
+        pairs = 0
+        for b in range(len(cq) - 1):
+            lq, lk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+            if not causal:
+                pairs += lq * lk
+            else:
+                pairs += sum(max(0, min(lk, i + lk - lq + 1)) for i in range(lq)) if lq < 4096 \
+                    else _causal_pairs(lq, lk)
+        return 2 * (192 + 128) * pairs * hq
+
+
+def _causal_pairs(lq: int, lk: int) -> int:
+    """sum_i clamp(i + lk - lq + 1, 0, lk) over i < lq, in closed form."""
+    total = 0
+    # rows with the full key set: i + lk - lq + 1 >= lk  <=>  i >= lq - 1
+    lo = max(0, lq - lk)                 # first row that sees at least one key: i >= lq - lk
+    full = lq - 1                        # only the last row sees every key when lq <= lk
+    if lo <= full:
+        n = full - lo                    # rows lo .. full - 1 see i + lk - lq + 1 keys
+        first = lo + lk - lq + 1
+        total += n * first + n * (n - 1) // 2
+    total += lk                          # the last row
+    return total
+
+
+def quantize_per_tensor(x: torch.Tensor):
+    """e4m3 codes of x / (amax / 448) and the descale amax / 448 (the page's recipe)."""
+    amax = float(x.abs().max().clamp_min(1e-30))
+    s = amax / E4M3_MAX
+    codes = (x / s).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, s
+
+
+def make_prefill_batch(lq: Sequence[int], lk: Sequence[int], num_q_heads: int, num_kv_heads: int,
+                       *, seed: int = 0, device: str = "cpu") -> PrefillBatch:
+    """Packed varlen fp8 prefill inputs: q, k, v ~ N(0, 1), each quantised per tensor to e4m3
+    with descale amax / 448 (the page's benchmark recipe)."""
+    if len(lq) != len(lk):
+        raise ValueError("lq and lk must have one entry per sequence")
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    tq, tk = sum(lq), sum(lk)
+    q, qd = quantize_per_tensor(torch.randn(tq, num_q_heads, 192, generator=g, device=dev))
+    k, kd = quantize_per_tensor(torch.randn(max(tk, 1), num_kv_heads, 192, generator=g, device=dev))
+    v, vd = quantize_per_tensor(torch.randn(max(tk, 1), num_kv_heads, 128, generator=g, device=dev))
+    k, v = k[:tk], v[:tk]
+    cq = torch.zeros(len(lq) + 1, dtype=torch.int32)
+    ck = torch.zeros(len(lk) + 1, dtype=torch.int32)
+    cq[1:] = torch.cumsum(torch.tensor(list(lq), dtype=torch.int32), 0)
+    ck[1:] = torch.cumsum(torch.tensor(list(lk), dtype=torch.int32), 0)
+    return PrefillBatch(q, k, v, cq.to(dev), ck.to(dev), qd, kd, vd, max(lq), max(lk))

@@ -4,6 +4,7 @@ the documented status codes before it touches any device state."""
 from __future__ import annotations
 
 import ctypes
+import glob
 import os
 import re
 
@@ -13,19 +14,24 @@ import torch
 from paged_fp8_speculative_gb300 import _lib, api
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mtpattn.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**([A-Za-z_]\w*)\s*\(", src, flags=re.M)
+    names = []
+    for header in HEADERS:
+        src = open(header).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**([A-Za-z_]\w*)\s*\(", src,
+                            flags=re.M)
+    return names
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert set(names) == set(_lib.SIGNATURES), names
-    assert "mtp_verify_attn_fwd" in names
+    assert len(names) == len(set(names))
+    assert "mtp_verify_attn_fwd" in names and "fmha_fwd_fp8_varlen" in names
 
 
 def test_library_exports_every_declared_symbol():
@@ -173,3 +179,56 @@ def test_static_wrapper_checks_shapes_before_the_call():
     for over in bad:
         with pytest.raises(ValueError):
             f(**(base | over))
+
+
+def prefill_call(**over):
+    a = dict(q=FAKE, qt=2 * 192, qh=192, k=FAKE, kt=192, kh=192, v=FAKE, vt=128, vh=128,
+             cq=FAKE, ck=FAKE, B=1, tq=4, tk=4, mq=4, mk=4, hq=2, hkv=1, qd=FAKE, kd=FAKE, vd=FAKE,
+             scale=0.07, causal=0, out=FAKE, ot=256, oh=128, lse=None, status=None, stream=None)
+    a.update(over)
+    return _lib.lib().fmha_fwd_fp8_varlen(
+        a["q"], a["qt"], a["qh"], a["k"], a["kt"], a["kh"], a["v"], a["vt"], a["vh"], a["cq"],
+        a["ck"], a["B"], a["tq"], a["tk"], a["mq"], a["mk"], a["hq"], a["hkv"], a["qd"], a["kd"],
+        a["vd"], a["scale"], a["causal"], a["out"], a["ot"], a["oh"], a["lse"], a["status"],
+        a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), api.E_ARG), (dict(cq=None), api.E_ARG), (dict(vd=None), api.E_ARG),
+    (dict(qt=200), api.E_ARG),                 # byte stride not a multiple of 16
+    (dict(vh=8), api.E_ARG),
+    (dict(ot=4), api.E_ARG),                   # element stride not a multiple of 8
+    (dict(q=FAKE + 8), api.E_ARG),             # base not 16-byte aligned
+    (dict(causal=2), api.E_ARG), (dict(B=-1), api.E_ARG), (dict(hq=0), api.E_ARG),
+    (dict(scale=float("nan")), api.E_ARG),
+    (dict(hq=3, hkv=2), api.E_UNSUPPORTED),
+])
+def test_prefill_refusals(over, code):
+    assert prefill_call(**over) == code
+
+
+def test_prefill_empty_batch_is_a_no_op():
+    assert prefill_call(B=0, tq=0) == api.OK
+    assert prefill_call(mq=0) == api.OK
+
+
+def test_prefill_wrapper_checks_shapes():
+    from paged_fp8_speculative_gb300 import synth
+    b = synth.make_prefill_batch([5, 3], [4, 6], 4, 2, seed=1)
+    f = api.fmha_fwd_fp8_varlen
+    base = dict(q=b.q, k=b.k, v=b.v, q_descale=b.q_descale, k_descale=b.k_descale,
+                v_descale=b.v_descale, cu_seqlens_q=b.cu_seqlens_q, cu_seqlens_k=b.cu_seqlens_k,
+                max_seqlen_q=5, max_seqlen_k=6)
+    for over in (dict(q=b.q[:, :, :128]), dict(v=b.k), dict(k=b.k[:, :1]),
+                 dict(cu_seqlens_k=b.cu_seqlens_k[:-1]), dict(cu_seqlens_q=b.cu_seqlens_q.long()),
+                 dict(out=torch.empty(8, 4, 128)), dict(q_descale=torch.ones(2))):
+        with pytest.raises(ValueError):
+            f(**(base | over))
+
+
+def test_prefill_causal_pair_count_closed_form():
+    """The flop count's closed form of the causal pairs against a direct sum."""
+    from paged_fp8_speculative_gb300.synth import _causal_pairs
+    for lq, lk in ((1, 1), (5, 3), (3, 5), (100, 100), (64, 300), (300, 64), (7, 0)):
+        direct = sum(max(0, min(lk, i + lk - lq + 1)) for i in range(lq))
+        assert _causal_pairs(lq, lk) == direct, (lq, lk)

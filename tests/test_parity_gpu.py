@@ -289,11 +289,13 @@ def test_planned_with_wide_block_table(det):
         api.mtp_verify_attn_set_deterministic(False)
 
 
-@pytest.mark.parametrize("nseq,hkv,S", [(100, 1, 16), (70, 2, 4), (150, 1, 2), (40, 4, 64)])
+@pytest.mark.parametrize("nseq,hkv,S", [(100, 1, 16), (70, 2, 4), (150, 1, 2), (40, 4, 64),
+                                        (32, 1, 16), (33, 1, 16), (16, 2, 64), (9, 1, 3)])
 def test_planned_many_units_ragged(nseq, hkv, S, sched):
     """Many (sequence, KV head) units with log-uniform lengths: the plan's general path (up to
     8 units per lane of the planning warp, the binary searches over the piece size and the
-    slots), and with more units than SMs (nseq x hkv = 160) the chunked fallback."""
+    slots), its 32-way searches for at most 32 units, and with more units than SMs
+    (nseq x hkv = 160) the chunked fallback."""
     ctx = synth.log_uniform_contexts(nseq, 6, 3000, seed=nseq + hkv)
     ql = synth.uniform_q_lens(nseq, 1, 4, seed=nseq + 7)
     ctx = [max(c, q) for c, q in zip(ctx, ql)]
