@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--ceiling-gib", type=float, default=4.0)
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip timing the other configurations after the headline one")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip timing the fp8 varlen prefill workload")
     return ap.parse_args()
 
 
@@ -202,6 +204,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": reasons, "samples_under_load": len(loaded), "samples": len(rows),
                 "power_w_max": max(r[2] for r in loaded)}
+
+
+def bf16_peak() -> tuple[float, str]:
+    """Dense bf16 tensor TFLOP/s measured on this machine (burst), else the stated fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
 
 
 def hbm_peak() -> tuple[float, str]:
@@ -359,6 +371,51 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
                      "clocks": clk}
         del b, tables, ws, out
         torch.cuda.empty_cache()
+    return res
+
+
+# fp8 varlen prefill (the second workload): the page's target shape, batch 1, 12288 queries
+# over 14336 keys, 96 query and KV heads, q/k head dim 192, v 128; causal and not.
+PREFILL_SHAPE = (1, 12288, 14336, 96, 96)
+
+
+def prefill_numbers(api, synth, warmup: int, uuid) -> dict:
+    """us/call and TFLOP/s of the prefill kernel on PREFILL_SHAPE (both products over the visible
+    pairs, as the page counts them), against the fp8 tensor peak: twice the measured bf16 rate
+    (the nominal fp8/bf16 ratio)."""
+    import torch
+    B, lq, lk, hq, hkv = PREFILL_SHAPE
+    b = synth.make_prefill_batch([lq] * B, [lk] * B, hq, hkv, seed=7, device="cuda")
+    out = torch.empty(b.q.shape[0], hq, 128, dtype=torch.bfloat16, device="cuda")
+    peak_bf16, kind = bf16_peak()
+    res = {"shape": {"batch": B, "seqlen_q": lq, "seqlen_k": lk, "heads_q": hq, "heads_kv": hkv,
+                     "head_dim_qk": 192, "head_dim_v": 128, "dtype": "e4m3 q/k/v, bf16 out"},
+           "peak_tflops": 2 * peak_bf16, "peak_source": f"2 x {kind} bf16_tflops"}
+    for causal in (False, True):
+        def call():
+            api.fmha_fwd_fp8_varlen(b.q, b.k, b.v, b.q_descale, b.k_descale, b.v_descale,
+                                    b.cu_seqlens_q, b.cu_seqlens_k, lq, lk, is_causal=causal,
+                                    out=out)
+        for _ in range(max(3, warmup // 4)):
+            call()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(uuid)
+        n = 10
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        flops = b.flops(causal)
+        tf = flops / (us * 1e-6) / 1e12
+        res["causal" if causal else "non_causal"] = {
+            "us_per_call": us, "tflops": tf, "flops": flops, "frac_of_peak": tf / (2 * peak_bf16),
+            "calls": n, "clocks": clk}
+    del b, out
+    torch.cuda.empty_cache()
     return res
 
 
@@ -523,6 +580,9 @@ def run_ours(a) -> None:
         del sets, h_q, h_bt, h_out
         torch.cuda.empty_cache()
         per_config = per_config_numbers(api, synth, dev, stream, peak, a.warmup, uuid)
+    prefill = None
+    if world == 1 and not a.no_prefill:
+        prefill = prefill_numbers(api, synth, a.warmup, uuid)
 
     us_call = 1e3 * ms / a.steps
     value = job_tbs(kv_bytes, world, a.steps, ms)
@@ -555,6 +615,8 @@ def run_ours(a) -> None:
         "clocks": clk,
         # every configuration, each timed like the headline one in this run (not part of value)
         "per_config": per_config,
+        # the second workload, fp8 varlen prefill attention (tensor-bound; not part of value)
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 

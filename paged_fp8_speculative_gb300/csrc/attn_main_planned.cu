@@ -173,107 +173,97 @@ __device__ Cursor plan_piece(const TcParams& prm, int lane, const PlanIn& in) {
     }
     return c;
   }
-  int total = 0;
+  // Unequal lengths.  This path runs once per call on every SM, so it is written for small
+  // code rather than for few instructions: its loops stay rolled over the lane's unit slots
+  // (fetching cold straight-line code cost more than the arithmetic), on copies of the
+  // per-slot values that may live in local memory.
+  int nl[8], Rl[8], pl[8], Ll[8], q0l[8], q1l[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) total += n[i];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-  auto pieces_total = [&](int c) -> int {    // sum_v ceil(n_v / c)
-    const float inv = 1.f / static_cast<float>(c);
-    int t = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < nb && n[i] > 0) t += ceil_div_inv(n[i], c, inv);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    return t;
-  };
-  // Bounds: sum_v ceil(n_v / c) >= total / c, and <= total / c + U, so the answer lies in
-  // [ceil(total / G), ceil(total / (G - U))]; no piece is cut below one 128-key tile, and a
-  // unit gets at most S pieces.
-  const int hi0 = max(maxn, 1);
-  int lo = max(max((total + G - 1) / G, (maxn + S - 1) / S), min(kPagesPerTile, hi0));
-  int hi = G > U ? min(hi0, (total + (G - U) - 1) / (G - U)) : hi0;
-  if (lo > hi0) lo = hi0;
-  if (hi < lo) hi = lo;
-  while (lo < hi) {
-    const int mid = (lo + hi) / 2;
-    if (pieces_total(mid) <= G) hi = mid;
-    else lo = mid + 1;
+  for (int i = 0; i < 8; ++i) {
+    nl[i] = n[i];
+    Ll[i] = Lv[i];
+    q0l[i] = q0v[i];
+    q1l[i] = q1v[i];
   }
-  int C = lo;
-  int pu[8];
-  int maxp = 0, npieces = 0;
-  auto count_pieces = [&]() {
-    const float invC = 1.f / static_cast<float>(C);
-    maxp = npieces = 0;
+  auto warp_sum = [](int x) -> int {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      pu[i] = (i < nb && n[i] > 0) ? ceil_div_inv(n[i], C, invC) : 0;
-      maxp = max(maxp, pu[i]);
-      npieces += pu[i];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
-      npieces += __shfl_xor_sync(0xffffffffu, npieces, o);
-    }
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
   };
-  count_pieces();
-  // Slot pool: when CTAs are left over and the caller let the library choose S, try sharing
-  // the workspace's rows x S partial slots out by length instead of capping every unit at S
-  // pieces: the smallest C (>= one tile) with sum_v ceil(n_v / C) <= grid and
-  // sum_v R_v ceil(n_v / C) within the pool, R_v the unit's query rows.  A C below the one
-  // above is feasible only if the S cap was binding; then the pool layout is used.  No unit
-  // has more pieces than CTAs (<= 256).
-  int R[8];
+  int total = 0;
+#pragma unroll 1
+  for (int i = 0; i < nb; ++i) total += nl[i];
+  total = warp_sum(total);
+  // sum_v ceil(n_v / c), and (weighted by the units' query rows) the row-slots it takes
+  auto count = [&](int c, int& rows_slots) -> int {
+    const float inv = 1.f / static_cast<float>(c);
+    int t = 0, w = 0;
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i)
+      if (nl[i] > 0) {
+        const int q = ceil_div_inv(nl[i], c, inv);
+        t += q;
+        w += Rl[i] * q;
+      }
+    rows_slots = warp_sum(w);
+    return warp_sum(t);
+  };
+#pragma unroll 1
+  for (int i = 0; i < nb; ++i) {
+    const int ql = q1l[i] - q0l[i];
+    Rl[i] = (nl[i] > 0 && q0l[i] >= 0 && q1l[i] <= p.total_q && ql >= 1 && ql <= kMaxQLen)
+                ? ql * p.ratio : 0;
+  }
+  // The smallest C with sum_v ceil(n_v / C) <= G (it lies in [ceil(total / G),
+  // ceil(total / (G - U))], since that sum is at most total / C + U), no piece below one
+  // 128-key tile, and at most S pieces per unit (C >= ceil(maxn / S)) -- or, with the slot
+  // pool allowed (the caller let the library choose S), with the rows x pieces within the
+  // pool instead of the S cap, when that gives a smaller C (the S cap was binding).
+  const int hi0 = max(maxn, 1);
+  const int lo_g = max((total + G - 1) / G, min(kPagesPerTile, hi0));
+  const int hi_g = G > U ? min(hi0, (total + (G - U) - 1) / (G - U)) : hi0;
+  const int lo_s = min(max(lo_g, (maxn + S - 1) / S), hi0);
+  const bool pool_ok = p.slot_pool && G <= 256;
+  int C = 0;
   bool pool = false;
-  if (p.slot_pool && npieces < G && G <= 256) {
-#pragma unroll
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    // pass 0: the S cap; pass 1 (slot pool): the row-slot capacity, below pass 0's C
+    int lo = pass == 0 ? lo_s : lo_g;
+    int hi = pass == 0 ? max(lo_s, hi_g) : C - 1;
+    if (pass == 1 && (!pool_ok || hi < lo)) break;
+    if (pass == 1) {                          // is anything below pass 0's C feasible at all?
+      int w;
+      if (count(hi, w) > G || w > p.pool_cap) break;
+    }
+    while (lo < hi) {
+      const int mid = (lo + hi) / 2;
+      int w;
+      const bool ok = count(mid, w) <= G && (pass == 0 || w <= p.pool_cap);
+      if (ok) hi = mid;
+      else lo = mid + 1;
+    }
+    C = lo;
+    pool = pass == 1;
+  }
+  int maxp = 0, npieces = 0;
+  {
+    const float invC = 1.f / static_cast<float>(C);
+#pragma unroll 1
     for (int i = 0; i < 8; ++i) {
-      R[i] = 0;
-      const int ql = q1v[i] - q0v[i];
-      if (i < nb && n[i] > 0 && q0v[i] >= 0 && q1v[i] <= p.total_q && ql >= 1 && ql <= kMaxQLen)
-        R[i] = ql * p.ratio;
+      pl[i] = (i < nb && nl[i] > 0) ? ceil_div_inv(nl[i], C, invC) : 0;
+      maxp = max(maxp, pl[i]);
+      npieces += pl[i];
     }
-    auto fits = [&](int c) -> bool {          // sum_v ceil(n_v / c) <= G and the rows fit
-      const float inv = 1.f / static_cast<float>(c);
-      int t = 0, w = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < nb && n[i] > 0) {
-          const int q = ceil_div_inv(n[i], c, inv);
-          t += q;
-          w += R[i] * q;
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        t += __shfl_xor_sync(0xffffffffu, t, o);
-        w += __shfl_xor_sync(0xffffffffu, w, o);
-      }
-      return t <= G && w <= p.pool_cap;
-    };
-    int lo2 = max((total + G - 1) / G, min(kPagesPerTile, hi0));
-    int hi2 = C - 1;
-    if (hi2 >= lo2 && fits(hi2)) {
-      while (lo2 < hi2) {
-        const int mid = (lo2 + hi2) / 2;
-        if (fits(mid)) hi2 = mid;
-        else lo2 = mid + 1;
-      }
-      C = lo2;
-      pool = true;
-      count_pieces();
-    }
+    for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+    npieces = warp_sum(npieces);
   }
   auto before = [&](int sl) -> int {         // pieces of slots below sl: sum_v min(p_v, sl)
     int t = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < nb) t += min(pu[i], sl);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    return t;
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i) t += min(pl[i], sl);
+    return warp_sum(t);
   };
   Cursor c;
   c.C = C;
@@ -283,37 +273,41 @@ __device__ Cursor plan_piece(const TcParams& prm, int lane, const PlanIn& in) {
   c.b = c.h = 0;
   c.pool = pool ? 1 : 0;
   c.off = 0;
+  c.L = c.q0 = c.q1 = 0;
   const int k = blockIdx.x;
   if (k >= npieces) {                        // more CTAs than pieces: nothing for this one
     c.k = prm.num_chunks;
     return c;
   }
   int slo = 0, shi = maxp - 1;               // largest slot sl with before(sl) <= k
+  int bslo = 0;                              // before(slo)
   while (slo < shi) {
     const int mid = (slo + shi + 1) / 2;
-    if (before(mid) <= k) slo = mid;
-    else shi = mid - 1;
+    const int bm = before(mid);
+    if (bm <= k) {
+      slo = mid;
+      bslo = bm;
+    } else {
+      shi = mid - 1;
+    }
   }
-  int r = k - before(slo);                   // the r-th unit (in order) that has slot slo
+  int r = k - bslo;                          // the r-th unit (in order) that has slot slo
   int u = -1, pu_u = 0;
-  c.L = c.q0 = c.q1 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < nb) {
-      const uint32_t m = __ballot_sync(0xffffffffu, pu[i] > slo);
-      const int cnt = __popc(m);
-      if (u < 0 && r < cnt) {
-        uint32_t mm = m;
-        for (int q = 0; q < r; ++q) mm &= mm - 1;        // drop the r lowest set bits
-        const int ln = __ffs(mm) - 1;
-        u = ln + 32 * i;
-        pu_u = __shfl_sync(0xffffffffu, pu[i], ln);
-        c.L = __shfl_sync(0xffffffffu, Lv[i], ln);
-        c.q0 = __shfl_sync(0xffffffffu, q0v[i], ln);
-        c.q1 = __shfl_sync(0xffffffffu, q1v[i], ln);
-      } else if (u < 0) {
-        r -= cnt;
-      }
+#pragma unroll 1
+  for (int i = 0; i < nb && u < 0; ++i) {
+    const uint32_t m = __ballot_sync(0xffffffffu, pl[i] > slo);
+    const int cnt = __popc(m);
+    if (r < cnt) {
+      uint32_t mm = m;
+      for (int q = 0; q < r; ++q) mm &= mm - 1;        // drop the r lowest set bits
+      const int ln = __ffs(mm) - 1;
+      u = ln + 32 * i;
+      pu_u = __shfl_sync(0xffffffffu, pl[i], ln);
+      c.L = __shfl_sync(0xffffffffu, Ll[i], ln);
+      c.q0 = __shfl_sync(0xffffffffu, q0l[i], ln);
+      c.q1 = __shfl_sync(0xffffffffu, q1l[i], ln);
+    } else {
+      r -= cnt;
     }
   }
   c.k = k;
@@ -324,12 +318,10 @@ __device__ Cursor plan_piece(const TcParams& prm, int lane, const PlanIn& in) {
   c.b = u - c.h * B;
   if (pool) {                                // the unit's first row-slot: sum_{v < u} R_v p_v
     int t = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < nb && lane + 32 * i < u) t += R[i] * pu[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    c.off = t;
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i)
+      if (lane + 32 * i < u) t += Rl[i] * pl[i];
+    c.off = warp_sum(t);
   }
   return c;
 }

@@ -31,6 +31,12 @@ namespace {
 
 constexpr int kGroup = 16;          // slots per warp
 
+__device__ __forceinline__ float ex2_approx(float x) {   // 2^x, hardware (rel. err ~2^-22)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(256)
 attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic
@@ -60,105 +66,83 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   // of weight 0 may hold anything, so its values are dropped by a select, never multiplied.
   const int n_spec = live ? max(0, min(min(p.slots_used, S) - s_lo, kGroup)) : 0;
   const float* lse = p.lse_part + (live ? row : 0) * S;
-  const float* o = p.o_part + ((live ? row : 0) * S + s_lo) * kHeadDim + part * 128 + lane * 4;
   const float l0 = live && lane < S ? lse[lane] : -INFINITY;
   const float l1 = live && lane + 32 < S ? lse[lane + 32] : -INFINITY;
+  const float* ob = p.o_part + (live ? row : 0) * S * kHeadDim + part * 128 + lane * 4;
   float4 a[kGroup];
 #pragma unroll
   for (int i = 0; i < kGroup; ++i)
-    if (i < n_spec) a[i] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(i) * kHeadDim);
-  int bad = isnan(l0) || isnan(l1);
-  float mx = fmaxf(l0, l1);
+    if (i < n_spec) a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s_lo + i) * kHeadDim);
+  // The row's slots: P of them, LSEs lv[k] of slots lane + 32 k on each lane, partial outputs
+  // from `ob`.  Slot pool (see AttnParams): the first LSE slot redirects to the row's partials
+  // (honoured only if this call allowed the pool, and only inside this call's pool; otherwise
+  // the row is treated as an error), which costs one more round trip; the loads above were
+  // speculative.
+  float lv[8];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    bad |= __shfl_xor_sync(0xffffffffu, bad, off);
+  for (int k = 0; k < 8; ++k) lv[k] = k == 0 ? l0 : (k == 1 ? l1 : -INFINITY);
+  int P = S;
+  int bad = 0;
+  bool spec = true;
+  if (live && p.slot_pool && __shfl_sync(0xffffffffu, __float_as_uint(l0), 0) == kPoolMarker) {
+    const int off = __shfl_sync(0xffffffffu, __float_as_int(l0), 1);
+    P = __shfl_sync(0xffffffffu, __float_as_int(l0), 2);
+    spec = false;
+    if (off < 0 || P < 1 || P > 256 || off > p.pool_cap - P) {
+      bad = 1;
+      P = 0;
+    } else {
+      const float* pl = p.pool_lse + off;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) lv[k] = lane + 32 * k < P ? pl[lane + 32 * k] : -INFINITY;
+      ob = p.o_part + static_cast<int64_t>(off) * kHeadDim + part * 128 + lane * 4;
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    bad |= isnan(lv[k]);
+    mx = fmaxf(mx, lv[k]);
+  }
+#pragma unroll
+  for (int off2 = 16; off2 > 0; off2 >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off2));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, off2);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  // Slot pool (see AttnParams): the row's first LSE slot redirects to its partials.  The
-  // loads above were speculative; the row costs one more round trip.
-  // Only this call's layout counts: a marker is honoured only if the call allowed the pool
-  // and its redirect lies inside this call's pool (else the row is treated as an error).
-  const bool pooled = live && p.slot_pool &&
-                      __shfl_sync(0xffffffffu, __float_as_uint(l0), 0) == kPoolMarker;
-  const int off = pooled ? __shfl_sync(0xffffffffu, __float_as_int(l0), 1) : 0;
-  const int P = pooled ? __shfl_sync(0xffffffffu, __float_as_int(l0), 2) : 0;
-  if (pooled && (off < 0 || P < 1 || P > 256 || off > p.pool_cap - P)) {
-    bad = 1;
-  } else if (pooled) {
-    const float* pl = p.pool_lse + off;
-    float lv[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) lv[k] = lane + 32 * k < P ? pl[lane + 32 * k] : -INFINITY;
-    bad = 0;
-    mx = -INFINITY;
+  if (!bad && mx != -INFINITY) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      bad |= isnan(lv[k]);
-      mx = fmaxf(mx, lv[k]);
+      lv[k] = lv[k] == -INFINITY ? 0.f : ex2_approx(lv[k] - mx);   // now the weights
+      wsum += lv[k];
     }
 #pragma unroll
-    for (int off2 = 16; off2 > 0; off2 >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off2));
-      bad |= __shfl_xor_sync(0xffffffffu, bad, off2);
-    }
-    if (!bad && mx != -INFINITY) {
+    for (int off2 = 16; off2 > 0; off2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off2);
+    // This warp's blocks of 16 slots: g, g + groups, ... (each inside one lane group of 32).
+    // All the weights of a block first, then every load of the block at once.
+#pragma unroll 1
+    for (int s0 = s_lo; s0 < P; s0 += groups * kGroup) {
+      const int kk = s0 >> 5;
+      float src = lv[0];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        lv[k] = lv[k] == -INFINITY ? 0.f : exp2f(lv[k] - mx);    // now the weights
-        wsum += lv[k];
-      }
+      for (int k = 1; k < 8; ++k)
+        if (k == kk) src = lv[k];
+      float w[kGroup];
 #pragma unroll
-      for (int off2 = 16; off2 > 0; off2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off2);
-      // This warp's blocks of 16 slots: g, g + groups, ... (all 16 inside one lane group of 32).
-      const float* ob = p.o_part + static_cast<int64_t>(off) * kHeadDim + part * 128 + lane * 4;
-      for (int s0 = g * kGroup; s0 < P; s0 += groups * kGroup) {
-        const int kk = s0 >> 5;
-        float src = lv[0];
+      for (int i = 0; i < kGroup; ++i) w[i] = __shfl_sync(0xffffffffu, src, (s0 & 31) + i);
+      const int have = spec && s0 == s_lo ? n_spec : 0;     // already in flight
 #pragma unroll
-        for (int k = 1; k < 8; ++k)
-          if (k == kk) src = lv[k];
-        float w[kGroup];
+      for (int i = 0; i < kGroup; ++i)
+        if (i >= have && s0 + i < P && w[i] != 0.f)          // uniform across the warp
+          a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s0 + i) * kHeadDim);
+      // A slot of weight 0 may hold anything: its values are dropped by a select.
 #pragma unroll
-        for (int i = 0; i < kGroup; ++i) w[i] = __shfl_sync(0xffffffffu, src, (s0 & 31) + i);
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i)
-          if (s0 + i < P && w[i] != 0.f)
-            a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s0 + i) * kHeadDim);
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i) {
-          if (s0 + i < P && w[i] != 0.f) {
-            acc.x = fmaf(w[i], a[i].x, acc.x); acc.y = fmaf(w[i], a[i].y, acc.y);
-            acc.z = fmaf(w[i], a[i].z, acc.z); acc.w = fmaf(w[i], a[i].w, acc.w);
-          }
+      for (int i = 0; i < kGroup; ++i) {
+        if (s0 + i < P && w[i] != 0.f) {
+          acc.x = fmaf(w[i], a[i].x, acc.x); acc.y = fmaf(w[i], a[i].y, acc.y);
+          acc.z = fmaf(w[i], a[i].z, acc.z); acc.w = fmaf(w[i], a[i].w, acc.w);
         }
-      }
-    }
-  } else if (!bad && mx != -INFINITY) {
-    const float w0 = l0 == -INFINITY ? 0.f : exp2f(l0 - mx);
-    const float w1 = l1 == -INFINITY ? 0.f : exp2f(l1 - mx);
-    wsum = w0 + w1;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-    // All the weights first, then every remaining load of the group at once: with the loads
-    // in the loop that shuffles the weights out, each waited for the shuffles before it, and
-    // rows of many slots paid for that in latency.
-    float w[kGroup];
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
-      const int s2 = s_lo + i;
-      w[i] = __shfl_sync(0xffffffffu, s2 < 32 ? w0 : w1, s2 & 31);   // 0 for s2 >= S
-    }
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i)
-      if (i >= n_spec && w[i] != 0.f)                                 // uniform across the warp
-        a[i] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(i) * kHeadDim);
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
-      if (w[i] != 0.f) {
-        acc.x = fmaf(w[i], a[i].x, acc.x); acc.y = fmaf(w[i], a[i].y, acc.y);
-        acc.z = fmaf(w[i], a[i].z, acc.z); acc.w = fmaf(w[i], a[i].w, acc.w);
       }
     }
   }
