@@ -79,6 +79,16 @@ __device__ __forceinline__ int div_inv(int n, int d, float inv) {
   return q;
 }
 
+// ceil(x / c) for 0 <= x < 2^22 and 2 <= c < 2^22 with integer operations only, given
+// m = ceil(2^32 / c) (magic_of): the estimate umulhi(x + c - 1, m) is at most one too large.
+__device__ __forceinline__ uint32_t magic_of(int c) { return 0xFFFFFFFFu / static_cast<uint32_t>(c) + 1u; }
+__device__ __forceinline__ int ceil_div_magic(int x, int c, uint32_t m) {
+  const uint32_t y = static_cast<uint32_t>(x + c - 1);
+  uint32_t q = __umulhi(y, m);
+  if (q * static_cast<uint32_t>(c) > y) --q;
+  return static_cast<int>(q);
+}
+
 // The plan's inputs: lane l holds units l, l + 32, ... (seq_lens and the cu_seqlens_q pair of
 // each).  plan_load only issues the loads, so that other requests can go out while they fly.
 struct PlanIn {
@@ -213,6 +223,105 @@ __device__ Cursor plan_piece(const TcParams& prm, int lane, const PlanIn& in) {
     const int ql = q1l[i] - q0l[i];
     Rl[i] = (nl[i] > 0 && q0l[i] >= 0 && q1l[i] <= p.total_q && ql >= 1 && ql <= kMaxQLen)
                 ? ql * p.ratio : 0;
+  }
+  if (U <= 32) {
+    // At most one unit per lane: each lane tests its own candidate piece size against every
+    // unit (the units' values come by shuffle inside a rolled loop) and a ballot gives the
+    // first candidate that passes, so a search over N values takes log32(N) rounds and no
+    // chains of warp reductions.  Same plan as the loop below.
+    const bool pool_ok = p.slot_pool && G <= 256;
+    const int n_own = nl[0], R_own = Rl[0];
+    const int hi0s = max(maxn, 1);
+    const int lo_gs = max((total + G - 1) / G, min(kPagesPerTile, hi0s));
+    const int hi_gs = G > U ? min(hi0s, (total + (G - U) - 1) / (G - U)) : hi0s;
+    const int lo_ss = min(max(lo_gs, (maxn + S - 1) / S), hi0s);
+    // pass 0: smallest C in [lo_ss, max(lo_ss, hi_gs)] with sum_v ceil(n_v / C) <= G and
+    // max_v ceil(n_v / C) <= S (the top of the range passes);  pass 1 (slot pool): smallest C
+    // in [lo_gs, C0] with the sum <= G and sum_v R_v ceil(n_v / C) within the pool, C0 (pass 0's
+    // answer) counting as passing: an answer below C0 means the S cap was binding.
+    int Cs = 0;
+    bool pools = false;
+#pragma unroll 1
+    for (int pass = 0; pass < (pool_ok ? 2 : 1); ++pass) {
+      int lo = pass == 0 ? lo_ss : lo_gs;
+      int hi = pass == 0 ? max(lo_ss, hi_gs) : Cs;
+      while (lo < hi) {
+        const int step = (hi - lo + 32) / 32;                     // ceil((hi - lo + 1) / 32)
+        const int c = min(lo + (lane + 1) * step - 1, hi);        // lane 31's candidate is hi
+        const bool trivial = c >= hi || c >= maxn;                // passes by construction
+        const uint32_t mg = magic_of(max(c, 2));
+        int t = 0, w = 0, mx = 0;
+#pragma unroll 1
+        for (int v = 0; v < U; ++v) {                             // every lane, uniformly
+          const int nv = __shfl_sync(0xffffffffu, n_own, v);
+          const int rv = __shfl_sync(0xffffffffu, R_own, v);
+          const int q = nv > 0 ? ceil_div_magic(nv, max(c, 2), mg) : 0;
+          t += q;
+          w += rv * q;
+          mx = max(mx, q);
+        }
+        const bool ok = trivial || (t <= G && (pass == 1 ? w <= p.pool_cap : mx <= S));
+        const int f = __ffs(__ballot_sync(0xffffffffu, ok)) - 1;
+        const int cf = min(lo + (f + 1) * step - 1, hi);
+        lo = f == 0 ? lo : min(lo + f * step - 1, hi) + 1;
+        hi = cf;
+      }
+      if (pass == 1 && lo < Cs) pools = true;
+      if (pass == 0 || pools) Cs = lo;
+    }
+    const int p_own = (lane < U && n_own > 0) ? (Cs >= n_own ? 1 : ceil_div_magic(n_own, Cs, magic_of(Cs))) : 0;
+    const int npieces = warp_sum(p_own);
+    int maxp = p_own;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+    Cursor c;
+    c.C = Cs;
+    c.s = 0;
+    c.pu = 0;
+    c.u = 0;
+    c.b = c.h = 0;
+    c.pool = pools ? 1 : 0;
+    c.off = 0;
+    c.L = c.q0 = c.q1 = 0;
+    const int k = blockIdx.x;
+    if (k >= npieces) {                      // more CTAs than pieces: nothing for this one
+      c.k = prm.num_chunks;
+      return c;
+    }
+    // slot-major: the slot is the largest sl with sum_v min(p_v, sl) <= k
+    auto before = [&](int sl) -> int {
+      int t = 0;
+#pragma unroll 1
+      for (int v = 0; v < U; ++v) t += min(__shfl_sync(0xffffffffu, p_own, v), sl);
+      return t;
+    };
+    int lo = 0, hi = maxp - 1;               // before(0) = 0 <= k
+    while (lo < hi) {                        // largest sl in [lo, hi] with before(sl) <= k
+      const int step = (hi - lo + 32) / 32;
+      const int cand = min(lo + lane * step, hi);
+      const int f = 31 - __clz(__ballot_sync(0xffffffffu, before(cand) <= k));   // lane 0 passes
+      const int cf = min(lo + f * step, hi);
+      hi = f == 31 ? hi : min(lo + (f + 1) * step, hi) - 1;
+      lo = cf;
+    }
+    const int slot = lo;
+    int r = k;                               // minus the pieces of slots below: sum_v min(p_v, slot)
+#pragma unroll 1
+    for (int v = 0; v < U; ++v) r -= min(__shfl_sync(0xffffffffu, p_own, v), slot);
+    uint32_t m = __ballot_sync(0xffffffffu, p_own > slot);
+    for (int q = 0; q < r; ++q) m &= m - 1;  // drop the r lowest set bits
+    const int u = __ffs(m) - 1;
+    c.k = k;
+    c.u = u;
+    c.s = slot;
+    c.pu = __shfl_sync(0xffffffffu, p_own, u);
+    c.L = __shfl_sync(0xffffffffu, Ll[0], u);
+    c.q0 = __shfl_sync(0xffffffffu, q0l[0], u);
+    c.q1 = __shfl_sync(0xffffffffu, q1l[0], u);
+    c.h = div_inv(u, B, prm.inv_seqs);
+    c.b = u - c.h * B;
+    if (pools) c.off = warp_sum(lane < u ? R_own * p_own : 0);
+    return c;
   }
   // The smallest C with sum_v ceil(n_v / C) <= G (it lies in [ceil(total / G),
   // ceil(total / (G - U))], since that sum is at most total / C + U), no piece below one

@@ -26,10 +26,13 @@
 
 #include <math.h>
 
+#include <algorithm>
+
 namespace mtpattn {
 namespace {
 
 constexpr int kGroup = 16;          // slots per warp
+constexpr int kMaxGroups = 8;       // 2 warps each: 512 threads per CTA at most
 
 __device__ __forceinline__ float ex2_approx(float x) {   // 2^x, hardware (rel. err ~2^-22)
   float y;
@@ -37,7 +40,7 @@ __device__ __forceinline__ float ex2_approx(float x) {   // 2^x, hardware (rel. 
   return y;
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic
   // shared memory, requested only for S > 16.
@@ -169,7 +172,19 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
 
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  const int groups = (p.num_segments + kGroup - 1) / kGroup;
+  int groups = (p.num_segments + kGroup - 1) / kGroup;
+  // With the slot pool a row may have up to one slot per SM: more groups per row let such a
+  // row load its slots in fewer rounds (the row-major rows leave the extra warps idle), as long
+  // as the whole grid stays one wave: a CTA of g groups holds 1/g of an SM's registers at
+  // 128 per thread (8 groups, 512 threads, at most).
+  if (p.slot_pool && rows > 0) {
+    const int sms = device_sm_count(-1);
+    if (sms > 0) {
+      const int64_t fit = static_cast<int64_t>(kMaxGroups) * sms / rows;   // groups for one wave
+      const int want = std::min<int64_t>(kMaxGroups, std::min<int64_t>(fit, (sms + kGroup - 1) / kGroup));
+      groups = std::max(groups, want);
+    }
+  }
   const int rows_per_cta = groups == 1 ? 2 : 1;    // 128 threads for S <= 16, else 64 per group
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
