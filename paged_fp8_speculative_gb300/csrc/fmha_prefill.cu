@@ -4,10 +4,15 @@
 // varlen THD layout, bf16 output, optional log-sum-exp, causal bottom-right or not).
 //
 // Work: one CTA per (128-query tile, query head, sequence); for a causal call the tiles of a
-// head run last-to-first, so the heaviest tiles start first.  Roles (192 threads):
-//   warps 0-3  softmax: thread r owns query row r of the tile = TMEM lane r;
-//   warp 4     TMA: the Q tile once, then K tiles (128 keys) and V tiles into 3-stage rings;
-//   warp 5     MMA: one elected lane issues tcgen05.mma kind::f8f6f4 and the commits, and
+// head run last-to-first, so the heaviest tiles start first.  Roles (320 threads):
+//   warps 0-15 softmax, four groups of four warps: warp w owns query rows 32 (w % 4) .. +31
+//              (TMEM lanes; a warp may only reach the lanes of its own quarter) and group w / 4
+//              owns keys 32 (w / 4) .. +31 of every 128-key tile and output dims 32 (w / 4) ..
+//              +31.  The groups of a row exchange their maxima once per tile through shared
+//              memory, so all take the same decisions.  The softmax is issue bound, and four
+//              warps per SM sub-partition hide its latencies far better than one;
+//   warp 16    TMA: the Q tile once, then K tiles (128 keys) and V tiles into 3-stage rings;
+//   warp 17    MMA: one elected lane issues tcgen05.mma kind::f8f6f4 and the commits, and
 //              the warp owns the TMEM allocation.
 // A 192-byte q or k row is staged as two 128-byte-swizzled halves of 128 rows; the upper
 // half's columns 192..255 lie past the tensor's head dim, and TMA fills them with zeros,
@@ -21,8 +26,9 @@
 // long rows of comparable logits.
 //
 // TMEM: S double buffer at columns 0 and 128 (fp32), O_hi at 256..383, O_lo at 384..511.
-// The softmax writes a tile's P_hi codes into columns 0..31 of that tile's S buffer and P_lo
-// into columns 32..63 (4 codes per column), and PV takes A = P from TMEM.  The MMA warp
+// Group g writes its 32 keys' P_hi codes into columns 32 g .. 32 g + 7 of the tile's S buffer
+// and P_lo into 32 g + 8 .. + 15 (4 codes per column, inside the columns it read itself), and
+// PV takes A = P from TMEM.  The MMA warp
 // issues QK(j), PV(j-1), QK(j+1), ...: QK(j+2) reuses the buffer whose P(j) PV(j) reads, and
 // the MMAs of one thread execute in issue order.
 //
@@ -45,7 +51,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreadsP = 192;
+constexpr int kGroupsP = 4;                     // softmax groups of 4 warps
+constexpr int kColsP = 128 / kGroupsP;          // keys (and output dims) per group
+constexpr int kSoftmaxP = kGroupsP * 128;
+constexpr int kThreadsP = kSoftmaxP + 64;
+constexpr int kWarpTma = kSoftmaxP / 32, kWarpMma = kWarpTma + 1;
 constexpr int kBM = 128;                        // query rows per tile
 constexpr int kBN = 128;                        // keys per tile
 constexpr int kHalfP = 128 * 128;               // one 128-byte-wide half of 128 rows (16 KB)
@@ -57,7 +67,8 @@ constexpr int kOffQP = 0;
 constexpr int kOffKP = kOffQP + kQTile;
 constexpr int kOffVP = kOffKP + kStagesP * kKTile;
 constexpr int kOffBarP = kOffVP + kStagesP * kVTile;
-constexpr int kLayoutP = kOffBarP + 256;
+constexpr int kOffXP = kOffBarP + 256;          // [2 tile parities][groups][128 rows] floats
+constexpr int kLayoutP = kOffXP + 2 * kGroupsP * 128 * 4;
 constexpr int kSmemP = kLayoutP + 1024;         // + alignment slack
 constexpr int kTmemColsP = 512;
 constexpr int kOColP = 256;                     // O_hi; O_lo at kOColP + 128
@@ -85,6 +96,7 @@ struct PBars {
   uint64_t k_full[kStagesP], k_empty[kStagesP], v_full[kStagesP], v_empty[kStagesP];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t final_mma;
+  uint64_t xbar[4][2];              // row-quarter q, tile parity: the groups' exchange (4 x 32 arrivals)
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -169,7 +181,7 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
   volatile int* abort_flag = &bars.abort;
 
   // ---- set-up -----------------------------------------------------------------------------------
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars.tmem_base), kTmemColsP);
     tmem_relinquish();
   }
@@ -183,10 +195,12 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i]), kBM);
+      mbar_init(smem_u32(&bars.p_full[i]), kSoftmaxP);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
     mbar_init(smem_u32(&bars.final_mma), 1);
+    for (int q = 0; q < 4; ++q)
+      for (int par = 0; par < 2; ++par) mbar_init(smem_u32(&bars.xbar[q][par]), kGroupsP * 32);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -195,7 +209,7 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ===================================== TMA producer ==========================================
     if (lane == 0) {
       prefetch_tmap(&prm.tmap_q);
@@ -231,7 +245,7 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         mbar_wait(smem_u32(&bars.v_full[u % kStagesP]), (u / kStagesP) & 1, &no_abort);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ===================================== MMA issuer ============================================
     constexpr uint32_t kIdescQK = idesc_e4m3_f32(kBM, kBN, false);
     constexpr uint32_t kIdescPV = idesc_e4m3_f32(kBM, 128, true);
@@ -249,13 +263,14 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       tc_fence_after();
       if (leader) {
         const uint32_t p_tmem = tmem + (u & 1) * 128;
+        // keys 32 k .. 32 k + 31 (group k): P_hi at column 32 k, P_lo at 32 k + 8
 #pragma unroll
         for (int k = 0; k < kBN / 32; ++k)                 // O_hi += P_hi V
-          mma_f8_ts(tmem + kOColP, p_tmem + 8 * k, v_desc + ((st * kVTile + k * 4096) >> 4),
+          mma_f8_ts(tmem + kOColP, p_tmem + 32 * k, v_desc + ((st * kVTile + k * 4096) >> 4),
                     kIdescPV, (u > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < kBN / 32; ++k)                 // O_lo += P_lo V
-          mma_f8_ts(tmem + kOColP + 128, p_tmem + 32 + 8 * k,
+          mma_f8_ts(tmem + kOColP + 128, p_tmem + 32 * k + 8,
                     v_desc + ((st * kVTile + k * 4096) >> 4), kIdescPV, (u > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bars.v_empty[st]));
         mma_commit(smem_u32(&bars.pv_done[u & 1]));
@@ -289,14 +304,35 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     mbar_wait(smem_u32(&bars.final_mma), 0, &no_abort);
   } else {
     // ===================================== softmax (rows) ========================================
-    const int r = tid;                                        // query row of the tile, TMEM lane
+    const int quad = warp & 3;                                // TMEM lane quarter
+    const int grp = warp >> 2;                                // keys / dims kColsP grp .. + kColsP - 1
+    const int r = 32 * quad + lane;                           // query row of the tile, TMEM lane
     const int i = i0 + r;
     const bool valid = i < Lq;
     // last key index row i may see (within the sequence)
     const int lim = !valid ? -1 : (prm.causal ? min(Lk - 1, i + Lk - Lq) : Lk - 1);
     const float sl2 = prm.scale_log2 * __ldg(prm.q_descale) * __ldg(prm.k_descale);
     const float vd = __ldg(prm.v_descale);
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+    const uint32_t col0 = kColsP * grp;                       // this group's S / P / O columns
+    float* xch = reinterpret_cast<float*>(base + kOffXP);     // [parity][group][row]
+    // Exchange with the same row in the other groups (warps quad + 4 g): use k of parity slot
+    // par is its (k / 2)-th use; every wait is bounded, so a group that gave up (abort) cannot
+    // leave the others waiting.  Returns the maximum (is_max) or the sum over the groups.
+    auto exchange = [&](int use, float v, bool is_max, float& all) -> bool {
+      const int par = use & 1;
+      xch[(par * kGroupsP + grp) * 128 + r] = v;
+      mbar_arrive(smem_u32(&bars.xbar[quad][par]));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.xbar[quad][par]),
+                                                        (use >> 1) & 1, abort_flag));
+      all = xch[(par * kGroupsP) * 128 + r];
+#pragma unroll
+      for (int g2 = 1; g2 < kGroupsP; ++g2) {
+        const float o = xch[(par * kGroupsP + g2) * 128 + r];
+        all = is_max ? fmaxf(all, o) : all + o;
+      }
+      return ok;
+    };
     float m = -INFINITY, l = 0.f;
     bool alive = true;
     for (int j = 0; j < nt; ++j) {
@@ -306,27 +342,28 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         break;
       }
       tc_fence_after();
-      float s[128];
+      float s[kColsP];
       {
-        uint32_t v[4][32];
+        uint32_t v[32];
+        tmem_ld32(lane_addr + sb * 128 + col0, v);
+        tmem_ld_wait(v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + sb * 128 + 32 * c, v[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(v[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(v[c][e]) * sl2;
+        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]) * sl2;
       }
-      const int key0 = j * kBN;
-      if (key0 + kBN - 1 > lim) {
+      const int key0 = j * kBN + col0;
+      if (key0 + kColsP - 1 > lim) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
+        for (int e = 0; e < kColsP; ++e)
           if (key0 + e > lim) s[e] = -INFINITY;
       }
-      float mx = s[0];
+      float hm = s[0];
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, s[e]);
+      for (int e = 1; e < kColsP; ++e) hm = fmaxf(hm, s[e]);
+      float mx;                                               // the tile's row maximum
+      if (!exchange(j, hm, true, mx)) {
+        alive = false;
+        break;
+      }
       float alpha = 1.f;
       bool rescale = false;
       if (mx != -INFINITY && (m == -INFINITY || mx > m + kTau)) {
@@ -339,9 +376,9 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       const float moff = m == -INFINITY ? 0.f : kShift - m;   // all s are -inf while m is
       float psum = 0.f;
       {
-        uint32_t ph[32], pl[32];
+        uint32_t ph[8], pl[8];
 #pragma unroll
-        for (int w = 0; w < 32; ++w) {
+        for (int w = 0; w < 8; ++w) {
           const float p0 = ex2f(s[4 * w] + moff), p1 = ex2f(s[4 * w + 1] + moff);
           const float p2 = ex2f(s[4 * w + 2] + moff), p3 = ex2f(s[4 * w + 3] + moff);
           psum += (p0 + p1) + (p2 + p3);
@@ -351,12 +388,17 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
           pl[w] = pack_e4m3x4(16.f * (p0 - h0), 16.f * (p1 - h1), 16.f * (p2 - h2),
                               16.f * (p3 - h3));
         }
-        tmem_st32(lane_addr + sb * 128, ph);                 // P over the tile's scores
-        tmem_st32(lane_addr + sb * 128 + 32, pl);
+        uint32_t pw[16];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          pw[w] = ph[w];
+          pw[8 + w] = pl[w];
+        }
+        tmem_st16(lane_addr + sb * 128 + col0, pw);           // P_hi then P_lo of these keys
       }
-      l = l * alpha + psum;
+      l = l * alpha + psum;                                   // this group's share
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds the sum up to PV(j - 1): rescale it once that PV has completed.
+        // O holds the sum up to PV(j - 1): rescale this group's dims once that PV completed.
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]),
                                                ((j - 1) >> 1) & 1, abort_flag))) {
           alive = false;
@@ -364,13 +406,14 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {                         // O_hi and O_lo
+        for (int c = 0; c < 2; ++c) {                         // O_hi and O_lo
+          const uint32_t col = kOColP + 128 * c + col0;
           uint32_t o[32];
-          tmem_ld32(lane_addr + kOColP + 32 * c, o);
+          tmem_ld32(lane_addr + col, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_addr + kOColP + 32 * c, o);
+          tmem_st32(lane_addr + col, o);
         }
       }
       tmem_st_wait();
@@ -378,38 +421,38 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       mbar_arrive(smem_u32(&bars.p_full[sb]));
     }
     // ---- epilogue: out = v_descale * O / l, lse = (m + log2 l - kShift) ln 2 ---------------------
+    // (l is the sum of the groups' shares: they all took the same rescaling decisions)
+    if (alive && !exchange(nt, l, false, l)) alive = false;
     if (alive && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(nt - 1) & 1]),
                                                    ((nt - 1) >> 1) & 1, abort_flag))) {
       tc_fence_after();
       const float sc = l > 0.f ? vd / l : 0.f;
       const int64_t row = static_cast<int64_t>(q0) + i;
       uint4* dst = reinterpret_cast<uint4*>(prm.out + row * prm.out_stride_tok +
-                                            static_cast<int64_t>(h) * prm.out_stride_head);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32], ol[32];
-        tmem_ld32(lane_addr + kOColP + 32 * c, o);
-        tmem_ld32(lane_addr + kOColP + 128 + 32 * c, ol);
-        tmem_ld_wait(o);
-        tmem_ld_wait(ol);
-        if (valid) {
+                                            static_cast<int64_t>(h) * prm.out_stride_head +
+                                            col0);
+      uint32_t o[32], ol[32];
+      tmem_ld32(lane_addr + kOColP + col0, o);
+      tmem_ld32(lane_addr + kOColP + 128 + col0, ol);
+      tmem_ld_wait(o);
+      tmem_ld_wait(ol);
+      if (valid) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            o[e] = __float_as_uint(fmaf(__uint_as_float(ol[e]), 0.0625f, __uint_as_float(o[e])));
+        for (int e = 0; e < 32; ++e)
+          o[e] = __float_as_uint(fmaf(__uint_as_float(ol[e]), 0.0625f, __uint_as_float(o[e])));
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 v2 = __floats2bfloat162_rn(
-                  __uint_as_float(o[8 * q + 2 * e]) * sc, __uint_as_float(o[8 * q + 2 * e + 1]) * sc);
-              w[e] = *reinterpret_cast<const uint32_t*>(&v2);
-            }
-            dst[4 * c + q] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                __uint_as_float(o[8 * q + 2 * e]) * sc, __uint_as_float(o[8 * q + 2 * e + 1]) * sc);
+            w[e] = *reinterpret_cast<const uint32_t*>(&v2);
           }
+          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      if (valid && prm.lse)
+      if (valid && grp == 0 && prm.lse)
         prm.lse[static_cast<int64_t>(h) * prm.total_q + row] =
             l > 0.f ? (m + log2f(l) - kShift) * kLn2 : -INFINITY;
     }
@@ -420,7 +463,7 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) set_status(prm.status, MTPATTN_ERR_TIMEOUT);
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemColsP);
   }
