@@ -108,32 +108,32 @@ __device__ __forceinline__ float ex2f(float x) {   // 2^x, hardware approximatio
   return y;
 }
 
-// Four e4m3 codes of a0..a3 (a0 in the lowest byte), round to nearest, saturating.
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
-  uint32_t w;
-  asm("{\n .reg .b16 lo, hi;\n"
-      " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
-      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
-      " mov.b32 %0, {lo, hi};\n}\n"
-      : "=r"(w)
-      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
-  return w;
-}
-
-// The four e4m3 codes of a word (lowest byte first) as floats, exactly: a code's 7 magnitude
-// bits placed at float bits 20..26 read as 2^-120 times its value (the e4m3 subnormals land on
-// float subnormals), so one multiply by 2^120 (not flushed to zero) rescales them.
-__device__ __forceinline__ void unpack_e4m3x4(uint32_t w, float& a0, float& a1, float& a2,
-                                              float& a3) {
-  const float k2p120 = 1.329227995784916e36f;   // 2^120
-  auto one = [&](uint32_t c) -> float {
-    const uint32_t bits = ((c & 0x7Fu) << 20) | ((c & 0x80u) << 24);
-    return __fmul_rn(__uint_as_float(bits), k2p120);
-  };
-  a0 = one(w & 0xFFu);
-  a1 = one((w >> 8) & 0xFFu);
-  a2 = one((w >> 16) & 0xFFu);
-  a3 = one(w >> 24);
+// The two-term e4m3 encoding of four probabilities p0..p3 (f32): hw = e4m3(p) (4 codes, lowest
+// byte first) and lw = e4m3(16 (p - hi)), formed in f16x2 arithmetic: p rounded to f16 keeps
+// 11 significant bits, hi decodes exactly into f16 (every e4m3 value is an f16 normal) and
+// p - hi is exact in f16 (|p - hi| <= p / 16), so the pair carries p to f16's precision.
+__device__ __forceinline__ void p_encode4(float p0, float p1, float p2, float p3, uint32_t& hw,
+                                          uint32_t& lw) {
+  asm("{\n .reg .b32 p01, p23, g01, g23, s16;\n"
+      " .reg .b16 a, b, c, d;\n"
+      " cvt.rn.f16x2.f32 p01, %3, %2;\n"
+      " cvt.rn.f16x2.f32 p23, %5, %4;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 a, p01;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 b, p23;\n"
+      " cvt.rn.f16x2.e4m3x2 g01, a;\n"
+      " cvt.rn.f16x2.e4m3x2 g23, b;\n"
+      " mov.b32 s16, 0x4C004C00;\n"
+      " sub.rn.f16x2 g01, p01, g01;\n"
+      " sub.rn.f16x2 g23, p23, g23;\n"
+      " mul.rn.f16x2 g01, g01, s16;\n"
+      " mul.rn.f16x2 g23, g23, s16;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 c, g01;\n"
+      " cvt.rn.satfinite.e4m3x2.f16x2 d, g23;\n"
+      " mov.b32 %0, {a, b};\n"
+      " mov.b32 %1, {c, d};\n"
+      "}\n"
+      : "=r"(hw), "=r"(lw)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
 }
 
 __global__ void __launch_bounds__(kThreadsP, 1)
@@ -342,23 +342,38 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         break;
       }
       tc_fence_after();
-      float s[kColsP];
+      float s[kColsP];                                        // raw logits <q, k> (unscaled)
       {
         uint32_t v[32];
         tmem_ld32(lane_addr + sb * 128 + col0, v);
         tmem_ld_wait(v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]) * sl2;
+        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]);
       }
       const int key0 = j * kBN + col0;
-      if (key0 + kColsP - 1 > lim) {
+      const bool masked = key0 + kColsP - 1 > lim;            // some key past the row's reach
+      if (masked) {                                           // out of the maximum below
 #pragma unroll
         for (int e = 0; e < kColsP; ++e)
-          if (key0 + e > lim) s[e] = -INFINITY;
+          if (key0 + e > lim) s[e] = sl2 >= 0.f ? -INFINITY : INFINITY;
       }
-      float hm = s[0];
+      // the largest scaled logit: sl2 times the largest (sl2 >= 0) or smallest raw one
+      float hm;
+      if (sl2 >= 0.f) {
+        float a = fmaxf(s[0], s[1]), b = fmaxf(s[2], s[3]);
 #pragma unroll
-      for (int e = 1; e < kColsP; ++e) hm = fmaxf(hm, s[e]);
+        for (int e = 4; e < kColsP; e += 4) {
+          a = fmaxf(a, fmaxf(s[e], s[e + 1]));
+          b = fmaxf(b, fmaxf(s[e + 2], s[e + 3]));
+        }
+        hm = fmaxf(a, b) * sl2;
+      } else {
+        float a = s[0];
+#pragma unroll
+        for (int e = 1; e < kColsP; ++e) a = fminf(a, s[e]);
+        hm = a * sl2;
+      }
+      if (hm != hm) hm = -INFINITY;                           // 0 * inf (sl2 = 0, masked)
       float mx;                                               // the tile's row maximum
       if (!exchange(j, hm, true, mx)) {
         alive = false;
@@ -374,26 +389,29 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         m = mx;
       }
       const float moff = m == -INFINITY ? 0.f : kShift - m;   // all s are -inf while m is
-      float psum = 0.f;
+      float psum;
       {
-        uint32_t ph[8], pl[8];
+        // p = 2^(sl2 s + kShift - m); masked keys get 2^-inf = 0
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const float p0 = ex2f(s[4 * w] + moff), p1 = ex2f(s[4 * w + 1] + moff);
-          const float p2 = ex2f(s[4 * w + 2] + moff), p3 = ex2f(s[4 * w + 3] + moff);
-          psum += (p0 + p1) + (p2 + p3);
-          ph[w] = pack_e4m3x4(p0, p1, p2, p3);
-          float h0, h1, h2, h3;
-          unpack_e4m3x4(ph[w], h0, h1, h2, h3);
-          pl[w] = pack_e4m3x4(16.f * (p0 - h0), 16.f * (p1 - h1), 16.f * (p2 - h2),
-                              16.f * (p3 - h3));
+        for (int e = 0; e < kColsP; ++e) s[e] = fmaf(s[e], sl2, moff);
+        if (masked) {
+#pragma unroll
+          for (int e = 0; e < kColsP; ++e)
+            if (key0 + e > lim) s[e] = -INFINITY;
         }
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int e = 0; e < kColsP; e += 2) {
+          s[e] = ex2f(s[e]);
+          s[e + 1] = ex2f(s[e + 1]);
+          a += s[e];
+          b += s[e + 1];
+        }
+        psum = a + b;
         uint32_t pw[16];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          pw[w] = ph[w];
-          pw[8 + w] = pl[w];
-        }
+        for (int w = 0; w < 8; ++w)
+          p_encode4(s[4 * w], s[4 * w + 1], s[4 * w + 2], s[4 * w + 3], pw[w], pw[8 + w]);
         tmem_st16(lane_addr + sb * 128 + col0, pw);           // P_hi then P_lo of these keys
       }
       l = l * alpha + psum;                                   // this group's share
