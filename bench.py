@@ -58,6 +58,10 @@ def parse_args():
                     help="skip timing the other configurations after the headline one")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip timing the fp8 varlen prefill workload")
+    ap.add_argument("--only-prefill", action="store_true",
+                    help="time only the fp8 varlen prefill workload (prints its own JSON line)")
+    ap.add_argument("--prefill-shape", default=",".join(map(str, PREFILL_SHAPE)),
+                    help="batch,seqlen_q,seqlen_k,heads_q,heads_kv of the prefill timing")
     return ap.parse_args()
 
 
@@ -379,12 +383,12 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
 PREFILL_SHAPE = (1, 12288, 14336, 96, 96)
 
 
-def prefill_numbers(api, synth, warmup: int, uuid) -> dict:
-    """us/call and TFLOP/s of the prefill kernel on PREFILL_SHAPE (both products over the visible
+def prefill_numbers(api, synth, warmup: int, uuid, shape=PREFILL_SHAPE) -> dict:
+    """us/call and TFLOP/s of the prefill kernel on `shape` (both products over the visible
     pairs, as the page counts them), against the fp8 tensor peak: twice the measured bf16 rate
     (the nominal fp8/bf16 ratio)."""
     import torch
-    B, lq, lk, hq, hkv = PREFILL_SHAPE
+    B, lq, lk, hq, hkv = shape
     b = synth.make_prefill_batch([lq] * B, [lk] * B, hq, hkv, seed=7, device="cuda")
     out = torch.empty(b.q.shape[0], hq, 128, dtype=torch.bfloat16, device="cuda")
     peak_bf16, kind = bf16_peak()
@@ -569,6 +573,16 @@ def run_ours(a) -> None:
     if diff > 2 ** -7 * scale:
         raise RuntimeError(f"end-to-end output differs from the device loop's: {diff} (scale {scale})")
 
+    # Host time of one eager call through the public API (argument checks, pointer checks of
+    # the C entry, tensor-map cache, two launches), the GPU kept busy so no call waits.
+    torch.cuda.synchronize()
+    n_host = 200
+    h0 = time.perf_counter()
+    for i in range(n_host):
+        call(i)
+    host_us = (time.perf_counter() - h0) / n_host * 1e6
+    torch.cuda.synchronize()
+
     if world > 1:
         ms, ms_e2e = slowest_rank([ms, ms_e2e], dev)
         dist.destroy_process_group()
@@ -582,7 +596,8 @@ def run_ours(a) -> None:
         per_config = per_config_numbers(api, synth, dev, stream, peak, a.warmup, uuid)
     prefill = None
     if world == 1 and not a.no_prefill:
-        prefill = prefill_numbers(api, synth, a.warmup, uuid)
+        prefill = prefill_numbers(api, synth, a.warmup, uuid,
+                                  tuple(int(x) for x in a.prefill_shape.split(",")))
 
     us_call = 1e3 * ms / a.steps
     value = job_tbs(kv_bytes, world, a.steps, ms)
@@ -612,6 +627,8 @@ def run_ours(a) -> None:
                               "step's inputs go up and its output comes down beside the neighbouring "
                               "steps' compute"},
         "gpu_launches": 2 * a.steps,
+        # host cost of one eager call (python wrapper + C entry + launches; not in `value`)
+        "host_us_per_eager_call": host_us,
         "clocks": clk,
         # every configuration, each timed like the headline one in this run (not part of value)
         "per_config": per_config,
@@ -621,10 +638,21 @@ def run_ours(a) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_only(a) -> None:
+    import torch
+    from paged_fp8_speculative_gb300 import api, synth
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    shape = tuple(int(x) for x in a.prefill_shape.split(","))
+    res = prefill_numbers(api, synth, a.warmup, None, shape)
+    print(json.dumps({"workload": "fmha_fwd_fp8_varlen", "prefill": res}), flush=True)
+
+
 def main():
     a = parse_args()
     if a.impl == "reference":
         run_reference(a)
+    elif a.only_prefill:
+        run_prefill_only(a)
     else:
         run_ours(a)
 
