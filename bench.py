@@ -229,11 +229,22 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources with comments and blank space removed, so that a profile
-    summary stays attached to the code it measured when only comments change."""
+# The prefill kernel's translation unit; the verify kernels (main, reduce) build from the rest.
+PREFILL_SOURCES = ("fmha_prefill.cu",)
+
+
+def source_digest(kernel: str = "verify") -> str:
+    """Digest of a kernel's sources with comments and blank space removed, so that a profile
+    summary stays attached to the code it measured when only comments change.  "verify" covers
+    every csrc file but the prefill kernel's own; "prefill" covers that one and the headers
+    it includes."""
     h = hashlib.sha256()
     for path in sorted(glob.glob(os.path.join(ROOT, "paged_fp8_speculative_gb300", "csrc", "*"))):
+        name = os.path.basename(path)
+        if kernel == "verify" and name in PREFILL_SOURCES:
+            continue
+        if kernel == "prefill" and name not in PREFILL_SOURCES + ("common.cuh", "sm100.cuh"):
+            continue
         with open(path, encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)        # block comments

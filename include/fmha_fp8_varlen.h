@@ -14,11 +14,10 @@
  * log-sum-exp -inf.  The optional log-sum-exp is natural-log, laid out [H_q][total_q] (the
  * varlen layout the page states; the base is our reading).
  *
- * Precision: Q, K and V are the e4m3 inputs themselves.  The probabilities P (scaled by
- * 2^5 relative to a running row maximum, so the small probabilities of a long row stay
- * representable) enter the PV tensor-core products as two e4m3 terms, hi + lo / 16, which
- * keeps 8 significant bits (bf16's) of every weight within 2^-13 of the row's largest; one
- * e4m3 term alone would put about 4% of noise on every weight.  Accumulation is fp32.
+ * Precision: Q, K and V are the e4m3 inputs themselves (V is widened to f16 inside the
+ * kernel, exactly).  The probabilities P (scaled by 2^5 relative to a running row maximum)
+ * are rounded once to f16, 11 significant bits, and enter the PV tensor-core product as
+ * f16; one e4m3 P would put about 4% of noise on every weight.  Accumulation is fp32.
  *
  * Conventions are those of mtpattn.h: device pointers of the current device, no allocation,
  * no synchronisation, the descales read on the device (graph-capture safe), status codes

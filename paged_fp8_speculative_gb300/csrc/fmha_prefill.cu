@@ -4,38 +4,41 @@
 // varlen THD layout, bf16 output, optional log-sum-exp, causal bottom-right or not).
 //
 // Work: one CTA per (128-query tile, query head, sequence); for a causal call the tiles of a
-// head run last-to-first, so the heaviest tiles start first.  Roles (320 threads):
-//   warps 0-15 softmax, four groups of four warps: warp w owns query rows 32 (w % 4) .. +31
-//              (TMEM lanes; a warp may only reach the lanes of its own quarter) and group w / 4
-//              owns keys 32 (w / 4) .. +31 of every 128-key tile and output dims 32 (w / 4) ..
-//              +31.  The groups of a row exchange their maxima once per tile through shared
-//              memory, so all take the same decisions.  The softmax is issue bound, and four
-//              warps per SM sub-partition hide its latencies far better than one;
-//   warp 16    TMA: the Q tile once, then K tiles (128 keys) and V tiles into 3-stage rings;
-//   warp 17    MMA: one elected lane issues tcgen05.mma kind::f8f6f4 and the commits, and
-//              the warp owns the TMEM allocation.
+// head run last-to-first, so the heaviest tiles start first.  Roles (384 threads):
+//   warps 0-7   softmax, two sets of four warps: set s takes the key tiles j = s (mod 2) with
+//               its own running maximum, sum and O accumulator (split-K inside the CTA), and
+//               the two are merged by their log-sum-exps at the end.  Thread t of a set owns
+//               query row t (TMEM lane t: warp w reaches lanes 32 (w % 4) .. +31) and all 128
+//               keys of the set's tiles, so a row's maximum needs no exchange.  While one set
+//               works through a tile the tensor pipe runs the other set's products;
+//   warp 8      TMA: the Q tile once, then K tiles (128 keys) and e4m3 V tiles into 2-stage
+//               rings (stage s holds set s's tiles);
+//   warp 9      MMA: one elected lane issues the tcgen05.mma (kind::f8f6f4 for QK, kind::f16
+//               for PV) and the commits, and the warp owns the TMEM allocation;
+//   warps 10-11 widen each e4m3 V tile to f16 in shared memory (16 chunks of 16 bytes a
+//               thread), the PV operand, off the softmax warps' path.
+// 12 warps leave 168 registers a thread: a softmax thread keeps its row's 128 logits.
 // A 192-byte q or k row is staged as two 128-byte-swizzled halves of 128 rows; the upper
 // half's columns 192..255 lie past the tensor's head dim, and TMA fills them with zeros,
-// but QK only runs over bytes 0..191 (6 MMAs of K = 32).  The V tile is 128 keys x 128 bytes,
-// read MN-major as the B operand of PV.
+// but QK only runs over bytes 0..191 (6 MMAs of K = 32).  The f16 V tile is 128 keys x 128
+// dims, two 128-byte-swizzled atoms of 64 dims, read MN-major as the B operand of PV.
 //
-// Precision: Q, K and V are the e4m3 inputs themselves.  P keeps bf16-class precision as
-// two e4m3 terms, p = hi + lo / 16 (hi = e4m3(p), lo = e4m3(16 (p - hi))), each multiplied
-// with V by its own MMA into its own accumulator: O = O_hi + O_lo / 16.  A single e4m3 P
-// (4 significant bits) puts about 4% of noise on every weight, 0.2-0.3 std of error on
+// Precision: Q, K and V are the e4m3 inputs themselves (V widened to f16 exactly: every e4m3
+// value is an f16 normal or subnormal).  P is rounded once, to f16 (11 significant bits), and
+// multiplied with V by the f16 tensor-core product into an f32 accumulator.  A single e4m3 P
+// (4 significant bits) would put about 4% of noise on every weight, 0.2-0.3 std of error on
 // long rows of comparable logits.
 //
-// TMEM: S double buffer at columns 0 and 128 (fp32), O_hi at 256..383, O_lo at 384..511.
-// Group g writes its 32 keys' P_hi codes into columns 32 g .. 32 g + 7 of the tile's S buffer
-// and P_lo into 32 g + 8 .. + 15 (4 codes per column, inside the columns it read itself), and
-// PV takes A = P from TMEM.  The MMA warp
-// issues QK(j), PV(j-1), QK(j+1), ...: QK(j+2) reuses the buffer whose P(j) PV(j) reads, and
-// the MMAs of one thread execute in issue order.
+// TMEM: S buffer s (set s's tiles) at columns 128 s (fp32), O of set s at 256 + 128 s.  A row's
+// P (f16 pairs, keys 2c and 2c + 1 in column c) overwrites columns 0..63 of its S buffer,
+// which the thread has read, and PV takes A = P from TMEM.  The MMA warp issues QK(j),
+// PV(j-1), QK(j+1), ...: QK(j+2) reuses the buffer whose P(j) PV(j) reads, and the MMAs of
+// one thread execute in issue order, so S(j + 2) complete also means PV(j) complete.
 //
 // Online softmax in the log2 domain with a lazy reference m (raised, and O rescaled in TMEM,
 // only when a tile's row maximum exceeds it by more than kTau): p_s = 2^(s - m + kShift)
-// <= 2^8, so P fits e4m3 and a probability 2^-14 below the row's maximum is still a
-// non-zero code (the probability-underflow case of the aiter PR #7375 page's review).
+// <= 2^8, and a probability 2^-19 below the row's maximum still keeps all 11 significant bits
+// of an f16 (the probability-underflow case of the aiter PR #7375 page's review).
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -51,30 +54,35 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kGroupsP = 4;                     // softmax groups of 4 warps
-constexpr int kColsP = 128 / kGroupsP;          // keys (and output dims) per group
-constexpr int kSoftmaxP = kGroupsP * 128;
-constexpr int kThreadsP = kSoftmaxP + 64;
-constexpr int kWarpTma = kSoftmaxP / 32, kWarpMma = kWarpTma + 1;
+constexpr int kSets = 2;                        // softmax sets: set s takes the tiles j = s (mod 2)
+constexpr int kSetThreads = 128;                // one thread per query row
+constexpr int kSoftmaxP = kSets * kSetThreads;
+constexpr int kWarpTma = kSoftmaxP / 32, kWarpMma = kWarpTma + 1, kWarpConv = kWarpMma + 1;
+constexpr int kConvWarps = 2;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kThreadsP = kSoftmaxP + 64 + kConvThreads;
 constexpr int kBM = 128;                        // query rows per tile
 constexpr int kBN = 128;                        // keys per tile
 constexpr int kHalfP = 128 * 128;               // one 128-byte-wide half of 128 rows (16 KB)
 constexpr int kQTile = 2 * kHalfP;              // 32 KB
 constexpr int kKTile = 2 * kHalfP;              // 32 KB per K stage
-constexpr int kVTile = kHalfP;                  // 16 KB per V stage
-constexpr int kStagesP = 3;
+constexpr int kV8Tile = kHalfP;                 // 16 KB per e4m3 V stage
+constexpr int kV16Tile = 2 * kHalfP;            // 32 KB per f16 V stage (two 64-dim atoms)
+constexpr int kStagesP = 2;                     // K, e4m3 V and f16 V rings: stage j % 2
 constexpr int kOffQP = 0;
 constexpr int kOffKP = kOffQP + kQTile;
-constexpr int kOffVP = kOffKP + kStagesP * kKTile;
-constexpr int kOffBarP = kOffVP + kStagesP * kVTile;
-constexpr int kOffXP = kOffBarP + 256;          // [2 tile parities][groups][128 rows] floats
-constexpr int kLayoutP = kOffXP + 2 * kGroupsP * 128 * 4;
+constexpr int kOffV8P = kOffKP + kStagesP * kKTile;
+constexpr int kOffV16P = kOffV8P + kStagesP * kV8Tile;
+constexpr int kOffBarP = kOffV16P + kStagesP * kV16Tile;
+constexpr int kOffFP = kOffBarP + 256;          // [set][128 rows] final m, then l
+constexpr int kLayoutP = kOffFP + 2 * kSets * 128 * 4;
 constexpr int kSmemP = kLayoutP + 1024;         // + alignment slack
 constexpr int kTmemColsP = 512;
-constexpr int kOColP = 256;                     // O_hi; O_lo at kOColP + 128
+constexpr int kOColP = 256;                     // O of set s at kOColP + 128 s
 constexpr float kTau = 3.f;                     // lazy-rescale threshold (log2 units)
 constexpr float kShift = 8.f - kTau;            // p_s = 2^(s - m + kShift) <= 2^8
 constexpr float kLn2 = 0.6931471805599453f;
+static_assert(kStagesP == kSets, "set s owns stage s of every ring and S buffer s");
 
 struct PrefillParams {
   CUtensorMap tmap_q, tmap_k, tmap_v;
@@ -94,9 +102,10 @@ struct PrefillParams {
 struct PBars {
   uint64_t q_full;
   uint64_t k_full[kStagesP], k_empty[kStagesP], v_full[kStagesP], v_empty[kStagesP];
+  uint64_t v16_full[kStagesP];      // the f16 V of the stage's tile is written
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t final_mma;
-  uint64_t xbar[4][2];              // row-quarter q, tile parity: the groups' exchange (4 x 32 arrivals)
+  uint64_t fin;                     // both sets' final m and l are published
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -107,33 +116,76 @@ __device__ __forceinline__ float ex2f(float x) {   // 2^x, hardware approximatio
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (a0, a1) * (b0, b1) + (c0, c1), one instruction for the pair
+__device__ __forceinline__ void fma_x2(float& a0, float& a1, float b0, float b1, float c0,
+                                       float c1) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+      " mov.b64 rc, {%4, %5};\n fma.rn.f32x2 ra, ra, rb, rc;\n mov.b64 {%0, %1}, ra;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_x2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+      " add.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+// two f32 -> f16x2 (p0 in the low half: the lower K index of a TMEM A-operand cell)
+__device__ __forceinline__ uint32_t f16x2_of(float p0, float p1) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(d) : "f"(p1), "f"(p0));
+  return d;
+}
+// four e4m3 codes (lowest byte first) -> two f16x2 words, exactly
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
 
-// The two-term e4m3 encoding of four probabilities p0..p3 (f32): hw = e4m3(p) (4 codes, lowest
-// byte first) and lw = e4m3(16 (p - hi)), formed in f16x2 arithmetic: p rounded to f16 keeps
-// 11 significant bits, hi decodes exactly into f16 (every e4m3 value is an f16 normal) and
-// p - hi is exact in f16 (|p - hi| <= p / 16), so the pair carries p to f16's precision.
-__device__ __forceinline__ void p_encode4(float p0, float p1, float p2, float p3, uint32_t& hw,
-                                          uint32_t& lw) {
-  asm("{\n .reg .b32 p01, p23, g01, g23, s16;\n"
-      " .reg .b16 a, b, c, d;\n"
-      " cvt.rn.f16x2.f32 p01, %3, %2;\n"
-      " cvt.rn.f16x2.f32 p23, %5, %4;\n"
-      " cvt.rn.satfinite.e4m3x2.f16x2 a, p01;\n"
-      " cvt.rn.satfinite.e4m3x2.f16x2 b, p23;\n"
-      " cvt.rn.f16x2.e4m3x2 g01, a;\n"
-      " cvt.rn.f16x2.e4m3x2 g23, b;\n"
-      " mov.b32 s16, 0x4C004C00;\n"
-      " sub.rn.f16x2 g01, p01, g01;\n"
-      " sub.rn.f16x2 g23, p23, g23;\n"
-      " mul.rn.f16x2 g01, g01, s16;\n"
-      " mul.rn.f16x2 g23, g23, s16;\n"
-      " cvt.rn.satfinite.e4m3x2.f16x2 c, g01;\n"
-      " cvt.rn.satfinite.e4m3x2.f16x2 d, g23;\n"
-      " mov.b32 %0, {a, b};\n"
-      " mov.b32 %1, {c, d};\n"
-      "}\n"
-      : "=r"(hw), "=r"(lw)
-      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
+// 32 lanes x 16 columns of 32 bits: thread t of the warp gets lane (base lane + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+// tcgen05.mma kind::f16 (f16 x f16 -> f32), A from tensor memory, B from shared memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of kind::f16 with f16 A and B and an f32 accumulator: the fields of
+// the kind::f8f6f4 descriptor, where format code 0 is f16 (and e4m3 there).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+  return idesc_e4m3_f32(M, N, b_mn_major);
 }
 
 __global__ void __launch_bounds__(kThreadsP, 1)
@@ -191,16 +243,16 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       mbar_init(smem_u32(&bars.k_full[i]), 1);
       mbar_init(smem_u32(&bars.k_empty[i]), 1);
       mbar_init(smem_u32(&bars.v_full[i]), 1);
-      mbar_init(smem_u32(&bars.v_empty[i]), 1);
+      mbar_init(smem_u32(&bars.v_empty[i]), kConvWarps);        // one arrival per converter warp
+      mbar_init(smem_u32(&bars.v16_full[i]), kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_full[i]), kSoftmaxP);
+      mbar_init(smem_u32(&bars.p_full[i]), kSetThreads);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
     mbar_init(smem_u32(&bars.final_mma), 1);
-    for (int q = 0; q < 4; ++q)
-      for (int par = 0; par < 2; ++par) mbar_init(smem_u32(&bars.xbar[q][par]), kGroupsP * 32);
+    mbar_init(smem_u32(&bars.fin), kSoftmaxP);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -234,8 +286,8 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
           break;
         }
         const uint32_t vb = smem_u32(&bars.v_full[st]);
-        mbar_arrive_expect_tx(vb, kVTile);
-        tma_load_3d(smem_u32(base + kOffVP + st * kVTile), &prm.tmap_v, vb, 0, hk, k0 + j * kBN);
+        mbar_arrive_expect_tx(vb, kV8Tile);
+        tma_load_3d(smem_u32(base + kOffV8P + st * kV8Tile), &prm.tmap_v, vb, 0, hk, k0 + j * kBN);
       }
       // Never leave with copies in flight (only after an abort can some be unconsumed).
       volatile int no_abort = 0;
@@ -248,31 +300,30 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
   } else if (warp == kWarpMma) {
     // ===================================== MMA issuer ============================================
     constexpr uint32_t kIdescQK = idesc_e4m3_f32(kBM, kBN, false);
-    constexpr uint32_t kIdescPV = idesc_e4m3_f32(kBM, 128, true);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kBM, 128, true);
     const uint64_t q_desc = sdesc_sw128(smem_u32(base + kOffQP), 16, 1024);
     const uint64_t k_desc = sdesc_sw128(smem_u32(base + kOffKP), 16, 1024);
-    const uint64_t v_desc = sdesc_sw128(smem_u32(base + kOffVP), kHalfP, 1024);
+    // f16 V: 64-dim atoms kHalfP apart (MN direction), 8-key groups 1024 bytes apart
+    const uint64_t v_desc = sdesc_sw128(smem_u32(base + kOffV16P), kHalfP, 1024);
     const bool leader = elect_one();
     auto wait_all = [&](uint64_t& bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort_flag));
     };
     auto issue_pv = [&](int u) -> bool {
-      const int st = u % kStagesP;
-      if (!wait_all(bars.v_full[st], (u / kStagesP) & 1)) return false;
+      // P(u) in TMEM and the f16 V(u) in shared memory
+      if (!wait_all(bars.v16_full[u & 1], (u >> 1) & 1)) return false;
       if (!wait_all(bars.p_full[u & 1], (u >> 1) & 1)) return false;
       tc_fence_after();
       if (leader) {
         const uint32_t p_tmem = tmem + (u & 1) * 128;
-        // keys 32 k .. 32 k + 31 (group k): P_hi at column 32 k, P_lo at 32 k + 8
+        const uint32_t v_off = (u & 1) * kV16Tile;
+        // keys 16 k .. 16 k + 15: P at columns 8 k .. 8 k + 7, V rows 16 k .. 16 k + 15
+        // (128 bytes each in both atoms); the set's own accumulator, first written by its
+        // first tile (u < 2)
 #pragma unroll
-        for (int k = 0; k < kBN / 32; ++k)                 // O_hi += P_hi V
-          mma_f8_ts(tmem + kOColP, p_tmem + 32 * k, v_desc + ((st * kVTile + k * 4096) >> 4),
-                    kIdescPV, (u > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < kBN / 32; ++k)                 // O_lo += P_lo V
-          mma_f8_ts(tmem + kOColP + 128, p_tmem + 32 * k + 8,
-                    v_desc + ((st * kVTile + k * 4096) >> 4), kIdescPV, (u > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars.v_empty[st]));
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_f16_ts(tmem + kOColP + 128 * (u & 1), p_tmem + 8 * k,
+                     v_desc + ((v_off + k * 2048) >> 4), kIdescPV, (u > 1 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bars.pv_done[u & 1]));
       }
       __syncwarp();
@@ -302,10 +353,54 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     __syncwarp();
     volatile int no_abort = 0;
     mbar_wait(smem_u32(&bars.final_mma), 0, &no_abort);
+  } else if (warp >= kWarpConv) {
+    // ===================================== V widening ============================================
+    // Thread c handles chunk slot vc = c % 8 of keys c / 8 + 8 i (i = 0..15), all with the same
+    // key % 8, hence the same logical chunk vcl (dims 16 vcl .. + 15, swizzled) and the same
+    // positions of its two f16 halves in the 64-dim atoms.
+    const int ct = tid - kWarpConv * 32;
+    const int vk = ct >> 3, vc = ct & 7;
+    const int vcl = vc ^ (vk & 7);
+    const uint32_t v8_off = vk * 128 + vc * 16;
+    const uint32_t v16_off0 = (vcl >> 2) * kHalfP + vk * 128 + (((2 * (vcl & 3)) ^ (vk & 7)) << 4);
+    const uint32_t v16_off1 = (vcl >> 2) * kHalfP + vk * 128 + (((2 * (vcl & 3) + 1) ^ (vk & 7)) << 4);
+    for (int j = 0; j < nt; ++j) {
+      const int st = j & 1;
+      // V(j) landed, and the f16 slot is free once PV(j - 2) completed
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars.v_full[st]), (j >> 1) & 1, abort_flag) &&
+                          (j < 2 || mbar_wait(smem_u32(&bars.pv_done[st]), ((j - 2) >> 1) & 1,
+                                              abort_flag))))
+        break;
+      tc_fence_after();
+      const unsigned char* src = base + kOffV8P + st * kV8Tile + v8_off;
+      unsigned char* dst = base + kOffV16P + st * kV16Tile;
+      // all loads first: a store may alias a later load as far as the compiler knows, which
+      // would serialise load, widen and store chunk by chunk
+      uint4 a[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) a[c] = *reinterpret_cast<const uint4*>(src + c * 8 * 128);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint4 w0, w1;
+        widen4(a[c].x, w0.x, w0.y);
+        widen4(a[c].y, w0.z, w0.w);
+        widen4(a[c].z, w1.x, w1.y);
+        widen4(a[c].w, w1.z, w1.w);
+        *reinterpret_cast<uint4*>(dst + v16_off0 + c * 8 * 128) = w0;
+        *reinterpret_cast<uint4*>(dst + v16_off1 + c * 8 * 128) = w1;
+      }
+      fence_proxy_async_smem();        // visible to the tensor cores once v16_full is observed
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars.v16_full[st]));
+        mbar_arrive(smem_u32(&bars.v_empty[st]));
+      }
+    }
   } else {
     // ===================================== softmax (rows) ========================================
+    const int set = warp >> 2;                                // tiles j = set (mod 2), S buffer set
     const int quad = warp & 3;                                // TMEM lane quarter
-    const int grp = warp >> 2;                                // keys / dims kColsP grp .. + kColsP - 1
     const int r = 32 * quad + lane;                           // query row of the tile, TMEM lane
     const int i = i0 + r;
     const bool valid = i < Lq;
@@ -314,71 +409,67 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     const float sl2 = prm.scale_log2 * __ldg(prm.q_descale) * __ldg(prm.k_descale);
     const float vd = __ldg(prm.v_descale);
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-    const uint32_t col0 = kColsP * grp;                       // this group's S / P / O columns
-    float* xch = reinterpret_cast<float*>(base + kOffXP);     // [parity][group][row]
-    // Exchange with the same row in the other groups (warps quad + 4 g): use k of parity slot
-    // par is its (k / 2)-th use; every wait is bounded, so a group that gave up (abort) cannot
-    // leave the others waiting.  Returns the maximum (is_max) or the sum over the groups.
-    auto exchange = [&](int use, float v, bool is_max, float& all) -> bool {
-      const int par = use & 1;
-      xch[(par * kGroupsP + grp) * 128 + r] = v;
-      mbar_arrive(smem_u32(&bars.xbar[quad][par]));
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.xbar[quad][par]),
-                                                        (use >> 1) & 1, abort_flag));
-      all = xch[(par * kGroupsP) * 128 + r];
-#pragma unroll
-      for (int g2 = 1; g2 < kGroupsP; ++g2) {
-        const float o = xch[(par * kGroupsP + g2) * 128 + r];
-        all = is_max ? fmaxf(all, o) : all + o;
-      }
-      return ok;
-    };
+    const uint32_t s_addr = lane_addr + set * 128;            // the set's S (then P) columns
+    const uint32_t o_addr = lane_addr + kOColP + set * 128;
+    float* fin_m = reinterpret_cast<float*>(base + kOffFP);   // [set][row]
+    float* fin_l = fin_m + kSets * 128;
     float m = -INFINITY, l = 0.f;
     bool alive = true;
-    for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[sb]), (j >> 1) & 1, abort_flag))) {
+    int u = 0;                                                // the set's own tile count
+    for (int j = set; j < nt; j += kSets, ++u) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[set]), u & 1, abort_flag))) {
         alive = false;
         break;
       }
       tc_fence_after();
-      float s[kColsP];                                        // raw logits <q, k> (unscaled)
+      const int key0 = j * kBN;
+      const bool masked = key0 + kBN - 1 > lim;               // some key past the row's reach
+      // the row's 128 raw logits <q, k> (unscaled), one TMEM round trip
+      float s[kBN];
       {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + sb * 128 + col0, v);
-        tmem_ld_wait(v);
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        tmem_ld32(s_addr, v0);
+        tmem_ld32(s_addr + 32, v1);
+        tmem_ld32(s_addr + 64, v2);
+        tmem_ld32(s_addr + 96, v3);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        tmem_ld_wait(v2);
+        tmem_ld_wait(v3);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 32; ++e) {
+          s[e] = __uint_as_float(v0[e]);
+          s[32 + e] = __uint_as_float(v1[e]);
+          s[64 + e] = __uint_as_float(v2[e]);
+          s[96 + e] = __uint_as_float(v3[e]);
+        }
       }
-      const int key0 = j * kBN + col0;
-      const bool masked = key0 + kColsP - 1 > lim;            // some key past the row's reach
       if (masked) {                                           // out of the maximum below
 #pragma unroll
-        for (int e = 0; e < kColsP; ++e)
+        for (int e = 0; e < kBN; ++e)
           if (key0 + e > lim) s[e] = sl2 >= 0.f ? -INFINITY : INFINITY;
       }
       // the largest scaled logit: sl2 times the largest (sl2 >= 0) or smallest raw one
       float hm;
       if (sl2 >= 0.f) {
-        float a = fmaxf(s[0], s[1]), b = fmaxf(s[2], s[3]);
+        float a = fmaxf(s[0], s[1]), c = fmaxf(s[2], s[3]);
 #pragma unroll
-        for (int e = 4; e < kColsP; e += 4) {
-          a = fmaxf(a, fmaxf(s[e], s[e + 1]));
-          b = fmaxf(b, fmaxf(s[e + 2], s[e + 3]));
+        for (int e = 4; e < kBN; e += 4) {
+          a = max3f(a, s[e], s[e + 1]);
+          c = max3f(c, s[e + 2], s[e + 3]);
         }
-        hm = fmaxf(a, b) * sl2;
+        hm = fmaxf(a, c);
       } else {
-        float a = s[0];
+        float a = fminf(s[0], s[1]), c = fminf(s[2], s[3]);
 #pragma unroll
-        for (int e = 1; e < kColsP; ++e) a = fminf(a, s[e]);
-        hm = a * sl2;
+        for (int e = 4; e < kBN; e += 4) {
+          a = min3f(a, s[e], s[e + 1]);
+          c = min3f(c, s[e + 2], s[e + 3]);
+        }
+        hm = fminf(a, c);
       }
-      if (hm != hm) hm = -INFINITY;                           // 0 * inf (sl2 = 0, masked)
-      float mx;                                               // the tile's row maximum
-      if (!exchange(j, hm, true, mx)) {
-        alive = false;
-        break;
-      }
+      float mx = hm * sl2;                                    // the tile's row maximum
+      if (mx != mx) mx = -INFINITY;                           // 0 * inf (sl2 = 0, masked)
       float alpha = 1.f;
       bool rescale = false;
       if (mx != -INFINITY && (m == -INFINITY || mx > m + kTau)) {
@@ -389,90 +480,106 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         m = mx;
       }
       const float moff = m == -INFINITY ? 0.f : kShift - m;   // all s are -inf while m is
-      float psum;
-      {
-        // p = 2^(sl2 s + kShift - m); masked keys get 2^-inf = 0
+      // p = 2^(sl2 s + kShift - m), masked keys 2^-inf = 0; P (f16 pairs) over the S columns,
+      // 32 keys (16 columns) at a time
+      float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < kColsP; ++e) s[e] = fmaf(s[e], sl2, moff);
+      for (int h4 = 0; h4 < 4; ++h4) {
+#pragma unroll
+        for (int e = 32 * h4; e < 32 * h4 + 32; e += 2) fma_x2(s[e], s[e + 1], sl2, sl2, moff, moff);
         if (masked) {
 #pragma unroll
-          for (int e = 0; e < kColsP; ++e)
+          for (int e = 32 * h4; e < 32 * h4 + 32; ++e)
             if (key0 + e > lim) s[e] = -INFINITY;
         }
-        float a = 0.f, b = 0.f;
-#pragma unroll
-        for (int e = 0; e < kColsP; e += 2) {
-          s[e] = ex2f(s[e]);
-          s[e + 1] = ex2f(s[e + 1]);
-          a += s[e];
-          b += s[e + 1];
-        }
-        psum = a + b;
         uint32_t pw[16];
 #pragma unroll
-        for (int w = 0; w < 8; ++w)
-          p_encode4(s[4 * w], s[4 * w + 1], s[4 * w + 2], s[4 * w + 3], pw[w], pw[8 + w]);
-        tmem_st16(lane_addr + sb * 128 + col0, pw);           // P_hi then P_lo of these keys
-      }
-      l = l * alpha + psum;                                   // this group's share
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds the sum up to PV(j - 1): rescale this group's dims once that PV completed.
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(j - 1) & 1]),
-                                               ((j - 1) >> 1) & 1, abort_flag))) {
-          alive = false;
-          break;
+        for (int e = 32 * h4; e < 32 * h4 + 32; e += 4) {
+          s[e] = ex2f(s[e]);
+          s[e + 1] = ex2f(s[e + 1]);
+          s[e + 2] = ex2f(s[e + 2]);
+          s[e + 3] = ex2f(s[e + 3]);
+          add_x2(a0, a1, s[e], s[e + 1]);
+          add_x2(c0, c1, s[e + 2], s[e + 3]);
+          pw[(e - 32 * h4) / 2] = f16x2_of(s[e], s[e + 1]);
+          pw[(e - 32 * h4) / 2 + 1] = f16x2_of(s[e + 2], s[e + 3]);
         }
-        tc_fence_after();
+        tmem_st16(s_addr + 16 * h4, pw);
+      }
+      l = l * alpha + ((a0 + c0) + (a1 + c1));
+      if (u > 0 && __any_sync(0xffffffffu, rescale)) {
+        // the set's O holds its sum up to PV(j - 2), complete: QK(j) was issued after it
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {                         // O_hi and O_lo
-          const uint32_t col = kOColP + 128 * c + col0;
+        for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + col, o);
+          tmem_ld32(o_addr + 32 * c, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_addr + col, o);
+          tmem_st32(o_addr + 32 * c, o);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[sb]));
+      mbar_arrive(smem_u32(&bars.p_full[set]));
     }
-    // ---- epilogue: out = v_descale * O / l, lse = (m + log2 l - kShift) ln 2 ---------------------
-    // (l is the sum of the groups' shares: they all took the same rescaling decisions)
-    if (alive && !exchange(nt, l, false, l)) alive = false;
-    if (alive && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[(nt - 1) & 1]),
-                                                   ((nt - 1) >> 1) & 1, abort_flag))) {
+    // ---- epilogue: merge the two sets' (m, l, O); out = v_descale * O / l,
+    //      lse = (m + log2 l - kShift) ln 2 ----------------------------------------------------------
+    if (alive) {
+      fin_m[set * 128 + r] = m;
+      fin_l[set * 128 + r] = l;
+    }
+    mbar_arrive(smem_u32(&bars.fin));
+    const int n0 = (nt + 1) / 2, n1 = nt / 2;                 // tiles of set 0 and set 1
+    alive = alive && __all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&bars.fin), 0, abort_flag) &&
+                                    mbar_wait(smem_u32(&bars.pv_done[0]), (n0 - 1) & 1, abort_flag) &&
+                                    (n1 == 0 || mbar_wait(smem_u32(&bars.pv_done[1]), (n1 - 1) & 1,
+                                                          abort_flag)));
+    if (alive) {
       tc_fence_after();
-      const float sc = l > 0.f ? vd / l : 0.f;
+      const float m0 = fin_m[r], l0 = fin_l[r];
+      const float m1 = n1 > 0 ? fin_m[128 + r] : -INFINITY, l1 = n1 > 0 ? fin_l[128 + r] : 0.f;
+      const bool use0 = l0 > 0.f, use1 = l1 > 0.f;            // l > 0 implies a finite m
+      const float M = use0 && use1 ? fmaxf(m0, m1) : (use0 ? m0 : m1);
+      const float w0 = use0 ? ex2f(m0 - M) : 0.f, w1 = use1 ? ex2f(m1 - M) : 0.f;
+      const float L = w0 * l0 + w1 * l1;
+      const float sc = L > 0.f ? vd / L : 0.f;
+      // this thread writes dims 64 set .. 64 set + 63 of its row, 16 at a time
+      const uint32_t dcol = 64 * set;
       const int64_t row = static_cast<int64_t>(q0) + i;
       uint4* dst = reinterpret_cast<uint4*>(prm.out + row * prm.out_stride_tok +
-                                            static_cast<int64_t>(h) * prm.out_stride_head +
-                                            col0);
-      uint32_t o[32], ol[32];
-      tmem_ld32(lane_addr + kOColP + col0, o);
-      tmem_ld32(lane_addr + kOColP + 128 + col0, ol);
-      tmem_ld_wait(o);
-      tmem_ld_wait(ol);
-      if (valid) {
+                                            static_cast<int64_t>(h) * prm.out_stride_head + dcol);
+      const float s0 = w0 * sc, s1 = w1 * sc;
+#pragma unroll 1
+      for (int hh = 0; hh < 4; ++hh) {
+        uint32_t oa[16], ob[16];
+        tmem_ld16(lane_addr + kOColP + dcol + 16 * hh, oa);
+        tmem_ld16(lane_addr + kOColP + 128 + dcol + 16 * hh, ob);
+        tmem_ld16_wait(oa);
+        tmem_ld16_wait(ob);
+        if (valid) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          o[e] = __float_as_uint(fmaf(__uint_as_float(ol[e]), 0.0625f, __uint_as_float(o[e])));
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(
-                __uint_as_float(o[8 * q + 2 * e]) * sc, __uint_as_float(o[8 * q + 2 * e + 1]) * sc);
-            w[e] = *reinterpret_cast<const uint32_t*>(&v2);
+            for (int e = 0; e < 4; ++e) {
+              const int d = 8 * q + 2 * e;
+              // a set with no weight contributes nothing (its accumulator may be unwritten)
+              const float x0 = (use0 ? __uint_as_float(oa[d]) * s0 : 0.f) +
+                               (use1 ? __uint_as_float(ob[d]) * s1 : 0.f);
+              const float x1 = (use0 ? __uint_as_float(oa[d + 1]) * s0 : 0.f) +
+                               (use1 ? __uint_as_float(ob[d + 1]) * s1 : 0.f);
+              const __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+            dst[2 * hh + q] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      if (valid && grp == 0 && prm.lse)
+      if (valid && set == 0 && prm.lse)
         prm.lse[static_cast<int64_t>(h) * prm.total_q + row] =
-            l > 0.f ? (m + log2f(l) - kShift) * kLn2 : -INFINITY;
+            L > 0.f ? (M + log2f(L) - kShift) * kLn2 : -INFINITY;
     }
   }
 

@@ -2,13 +2,12 @@
 CPU oracle (oracle.prefill), through the C ABI.
 
 Tolerance.  Q, K and V are the e4m3 inputs themselves, so the kernel's roundings beyond
-float32 re-association are P and the bf16 output.  P enters the PV products as two e4m3
-terms, hi + lo / 16, which keeps bf16's 8 significant bits of every weight within 2^-13 of
-the row's largest, so the bound is the one stated for kernels whose Q and P stay bf16/fp32:
-max|gpu - oracle| / std(out) <= 0.01, after granting each element half a bf16 ulp of the
-exact value (oracle.excess_over_half_ulp).  (A single e4m3 P, 4 significant bits, measured
-0.26 std on the causal 1500 x 1800 case.)  The log-sum-exp is formed from the unrounded
-probabilities in float32 and must agree to 1e-3.
+float32 re-association are P and the bf16 output.  P enters the PV products as f16 (11
+significant bits, finer than bf16's 8), so the bound is the one stated for kernels whose Q
+and P stay bf16/fp32: max|gpu - oracle| / std(out) <= 0.01, after granting each element
+half a bf16 ulp of the exact value (oracle.excess_over_half_ulp).  (A single e4m3 P, 4
+significant bits, measured 0.26 std on the causal 1500 x 1800 case.)  The log-sum-exp is
+formed from the unrounded probabilities in float32 and must agree to 1e-3.
 """
 from __future__ import annotations
 
