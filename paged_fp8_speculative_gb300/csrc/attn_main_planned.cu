@@ -556,6 +556,9 @@ __device__ __forceinline__ Cursor first_cursor_of(const TcParams& prm, Bars& bar
   return c;
 }
 
+// The epilogue reads the partial output from TMEM two 64-column blocks per round trip.
+constexpr int kEpilogueBlocks = 2;
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_main_planned_kernel(const __grid_constant__ TcParams prm) {
 #include "attn_main_body.inc"

@@ -143,6 +143,10 @@ __device__ __forceinline__ Cursor first_cursor_of(const TcParams& prm, Bars&, in
   return cursor_first(prm);
 }
 
+// The epilogue reads the partial output from TMEM one 64-column block per round trip (two
+// would not fit this kernel's registers).
+constexpr int kEpilogueBlocks = 1;
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_main_tc_kernel(const __grid_constant__ TcParams prm) {
 #include "attn_main_body.inc"
