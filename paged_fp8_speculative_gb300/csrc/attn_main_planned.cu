@@ -235,45 +235,42 @@ __device__ Cursor plan_piece(const TcParams& prm, int lane, const PlanIn& in) {
     const int lo_gs = max((total + G - 1) / G, min(kPagesPerTile, hi0s));
     const int hi_gs = G > U ? min(hi0s, (total + (G - U) - 1) / (G - U)) : hi0s;
     const int lo_ss = min(max(lo_gs, (maxn + S - 1) / S), hi0s);
-    // pass 0: smallest C in [lo_ss, max(lo_ss, hi_gs)] with sum_v ceil(n_v / C) <= G and
-    // max_v ceil(n_v / C) <= S (the top of the range passes);  pass 1 (slot pool): smallest C
-    // in [lo_gs, C0] with the sum <= G and sum_v R_v ceil(n_v / C) within the pool, C0 (pass 0's
-    // answer) counting as passing: an answer below C0 means the S cap was binding.
-    int Cs = 0;
-    bool pools = false;
+    // The smallest C in [lo_gs (lo_ss without the pool), max(lo_ss, hi_gs)] with
+    // sum_v ceil(n_v / C) <= G and either max_v ceil(n_v / C) <= S (the row-major slots) or,
+    // with the slot pool allowed, sum_v R_v ceil(n_v / C) within the pool.  All three sums
+    // fall as C grows, so the condition holds from some C on (the top of the range passes)
+    // and one search finds it; the pool is used only where the S cap is what fails (max
+    // pieces > S, below).  This is the C of the two searches below (S cap, then pool).
+    int clo = pool_ok ? lo_gs : lo_ss;
+    int chi = max(lo_ss, hi_gs);
+    while (clo < chi) {
+      const int step = (chi - clo + 32) / 32;                     // ceil((chi - clo + 1) / 32)
+      const int c = min(clo + (lane + 1) * step - 1, chi);        // lane 31's candidate is chi
+      const bool trivial = c >= chi || c >= maxn;                  // passes by construction
+      const uint32_t mg = magic_of(max(c, 2));
+      int t = 0, w = 0, mx = 0;
 #pragma unroll 1
-    for (int pass = 0; pass < (pool_ok ? 2 : 1); ++pass) {
-      int lo = pass == 0 ? lo_ss : lo_gs;
-      int hi = pass == 0 ? max(lo_ss, hi_gs) : Cs;
-      while (lo < hi) {
-        const int step = (hi - lo + 32) / 32;                     // ceil((hi - lo + 1) / 32)
-        const int c = min(lo + (lane + 1) * step - 1, hi);        // lane 31's candidate is hi
-        const bool trivial = c >= hi || c >= maxn;                // passes by construction
-        const uint32_t mg = magic_of(max(c, 2));
-        int t = 0, w = 0, mx = 0;
-#pragma unroll 1
-        for (int v = 0; v < U; ++v) {                             // every lane, uniformly
-          const int nv = __shfl_sync(0xffffffffu, n_own, v);
-          const int rv = __shfl_sync(0xffffffffu, R_own, v);
-          const int q = nv > 0 ? ceil_div_magic(nv, max(c, 2), mg) : 0;
-          t += q;
-          w += rv * q;
-          mx = max(mx, q);
-        }
-        const bool ok = trivial || (t <= G && (pass == 1 ? w <= p.pool_cap : mx <= S));
-        const int f = __ffs(__ballot_sync(0xffffffffu, ok)) - 1;
-        const int cf = min(lo + (f + 1) * step - 1, hi);
-        lo = f == 0 ? lo : min(lo + f * step - 1, hi) + 1;
-        hi = cf;
+      for (int v = 0; v < U; ++v) {                               // every lane, uniformly
+        const int nv = __shfl_sync(0xffffffffu, n_own, v);
+        const int rv = __shfl_sync(0xffffffffu, R_own, v);
+        const int q = nv > 0 ? ceil_div_magic(nv, max(c, 2), mg) : 0;
+        t += q;
+        w += rv * q;
+        mx = max(mx, q);
       }
-      if (pass == 1 && lo < Cs) pools = true;
-      if (pass == 0 || pools) Cs = lo;
+      const bool ok = trivial || (t <= G && (mx <= S || (pool_ok && w <= p.pool_cap)));
+      const int f = __ffs(__ballot_sync(0xffffffffu, ok)) - 1;
+      const int cf = min(clo + (f + 1) * step - 1, chi);
+      clo = f == 0 ? clo : min(clo + f * step - 1, chi) + 1;
+      chi = cf;
     }
+    const int Cs = clo;
     const int p_own = (lane < U && n_own > 0) ? (Cs >= n_own ? 1 : ceil_div_magic(n_own, Cs, magic_of(Cs))) : 0;
     const int npieces = warp_sum(p_own);
     int maxp = p_own;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+    const bool pools = pool_ok && maxp > S;
     Cursor c;
     c.C = Cs;
     c.s = 0;
