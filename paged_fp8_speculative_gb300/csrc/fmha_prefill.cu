@@ -103,7 +103,7 @@ struct PBars {
   uint64_t q_full;
   uint64_t k_full[kStagesP], k_empty[kStagesP], v_full[kStagesP], v_empty[kStagesP];
   uint64_t v16_full[kStagesP];      // the f16 V of the stage's tile is written
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[2], p_half[2], p_full[2], pv_done[2];   // p_half: P of keys 0..63 written
   uint64_t final_mma;
   uint64_t fin;                     // both sets' final m and l are published
   uint32_t tmem_base;
@@ -248,6 +248,7 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_half[i]), kSetThreads);
       mbar_init(smem_u32(&bars.p_full[i]), kSetThreads);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
@@ -310,23 +311,28 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort_flag));
     };
     auto issue_pv = [&](int u) -> bool {
-      // P(u) in TMEM and the f16 V(u) in shared memory
+      // P(u) in TMEM and the f16 V(u) in shared memory; the products of keys 0..63 go out as
+      // soon as their half of P is written, while the softmax works on keys 64..127
+      const uint32_t p_tmem = tmem + (u & 1) * 128;
+      const uint32_t v_off = (u & 1) * kV16Tile;
       if (!wait_all(bars.v16_full[u & 1], (u >> 1) & 1)) return false;
-      if (!wait_all(bars.p_full[u & 1], (u >> 1) & 1)) return false;
-      tc_fence_after();
-      if (leader) {
-        const uint32_t p_tmem = tmem + (u & 1) * 128;
-        const uint32_t v_off = (u & 1) * kV16Tile;
-        // keys 16 k .. 16 k + 15: P at columns 8 k .. 8 k + 7, V rows 16 k .. 16 k + 15
-        // (128 bytes each in both atoms); the set's own accumulator, first written by its
-        // first tile (u < 2)
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        if (!wait_all(half == 0 ? bars.p_half[u & 1] : bars.p_full[u & 1], (u >> 1) & 1))
+          return false;
+        tc_fence_after();
+        if (leader) {
+          // keys 16 k .. 16 k + 15: P at columns 8 k .. 8 k + 7, V rows 16 k .. 16 k + 15
+          // (128 bytes each in both atoms); the set's own accumulator, first written by its
+          // first tile (u < 2)
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          mma_f16_ts(tmem + kOColP + 128 * (u & 1), p_tmem + 8 * k,
-                     v_desc + ((v_off + k * 2048) >> 4), kIdescPV, (u > 1 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars.pv_done[u & 1]));
+          for (int k = 4 * half; k < 4 * half + 4; ++k)
+            mma_f16_ts(tmem + kOColP + 128 * (u & 1), p_tmem + 8 * k,
+                       v_desc + ((v_off + k * 2048) >> 4), kIdescPV, (u > 1 || k > 0) ? 1u : 0u);
+          if (half == 1) mma_commit(smem_u32(&bars.pv_done[u & 1]));
+        }
+        __syncwarp();
       }
-      __syncwarp();
       return true;
     };
     bool ok = wait_all(bars.q_full, 0);
@@ -480,8 +486,21 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         m = mx;
       }
       const float moff = m == -INFINITY ? 0.f : kShift - m;   // all s are -inf while m is
+      if (u > 0 && __any_sync(0xffffffffu, rescale)) {
+        // the set's O holds its sum up to PV(j - 2), complete: QK(j) was issued after it; the
+        // first products of this tile may start once P's first half is signalled below
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {                      // 16 columns at a time: the row's
+          uint32_t o[16];                                 // logits are live meanwhile
+          tmem_ld16(o_addr + 16 * c, o);
+          tmem_ld16_wait(o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(o_addr + 16 * c, o);
+        }
+      }
       // p = 2^(sl2 s + kShift - m), masked keys 2^-inf = 0; P (f16 pairs) over the S columns,
-      // 32 keys (16 columns) at a time
+      // 32 keys (16 columns) at a time; keys 0..63 are signalled on their own (p_half)
       float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
 #pragma unroll
       for (int h4 = 0; h4 < 4; ++h4) {
@@ -505,20 +524,13 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
           pw[(e - 32 * h4) / 2 + 1] = f16x2_of(s[e + 2], s[e + 3]);
         }
         tmem_st16(s_addr + 16 * h4, pw);
-      }
-      l = l * alpha + ((a0 + c0) + (a1 + c1));
-      if (u > 0 && __any_sync(0xffffffffu, rescale)) {
-        // the set's O holds its sum up to PV(j - 2), complete: QK(j) was issued after it
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + 32 * c, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(o_addr + 32 * c, o);
+        if (h4 == 1) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.p_half[set]));
         }
       }
+      l = l * alpha + ((a0 + c0) + (a1 + c1));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[set]));
