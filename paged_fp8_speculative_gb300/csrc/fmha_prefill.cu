@@ -33,7 +33,9 @@
 // P (f16 pairs, keys 2c and 2c + 1 in column c) overwrites columns 0..63 of its S buffer,
 // which the thread has read, and PV takes A = P from TMEM.  The MMA warp issues QK(j),
 // PV(j-1), QK(j+1), ...: QK(j+2) reuses the buffer whose P(j) PV(j) reads, and the MMAs of
-// one thread execute in issue order, so S(j + 2) complete also means PV(j) complete.
+// one thread execute in issue order, so S(j + 2) complete also means PV(j) complete.  PV(j)
+// goes out in two halves: keys 0..63 once the set signals that half of P (p_half), while it
+// computes keys 64..127, and keys 64..127 at p_full.
 //
 // Online softmax in the log2 domain with a lazy reference m (raised, and O rescaled in TMEM,
 // only when a tile's row maximum exceeds it by more than kTau): p_s = 2^(s - m + kShift)
