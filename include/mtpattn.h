@@ -98,12 +98,16 @@ int32_t mtp_verify_attn_num_segments(int32_t num_seqs, int32_t num_kv_heads,
 
 /*
  * Bytes of device workspace mtp_verify_attn_fwd needs (the library's own sizing
- * rule; the pages print no counterpart): a 4096-byte header of
- * tile counters (one per (sequence, KV head) unit, up to 1024 units), then
- * float32 partial log-sum-exps [total_q * num_q_heads][num_segments], then
- * float32 partial outputs [total_q * num_q_heads][num_segments][256], each region
- * 256-byte aligned.  Returns 0 for invalid arguments.
+ * rule; the pages print no counterpart): a header of MTPATTN_WORKSPACE_HEADER_BYTES
+ * (4096 bytes of tile counters, one per (sequence, KV head) unit up to 1024 units,
+ * then two 32-bit call counters: the main kernel's CTAs count themselves in when
+ * they start and out after their last write, and the reduce merges once the two
+ * agree), then float32 partial log-sum-exps [total_q * num_q_heads][num_segments],
+ * then float32 partial outputs [total_q * num_q_heads][num_segments][256], each
+ * region 256-byte aligned.  Returns 0 for invalid arguments.
  */
+#define MTPATTN_WORKSPACE_HEADER_BYTES 4352
+
 size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int32_t num_segments);
 
 /*
@@ -127,12 +131,13 @@ size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_heads, int3
  *               most one per SM) when short ones use fewer.  A ragged batch with one long
  *               sequence then streams it on every SM instead of on S of them.
  *  workspace    device, >= mtp_verify_attn_workspace_size(...) bytes, 256-byte aligned.
- *               Its first 4096 bytes (the counter header) must be zero before the
- *               workspace's first use (e.g. one cudaMemset); every call that returns
- *               MTPATTN_OK, also one that reports a device error, leaves them zero, so
- *               the workspace can be reused by calls of any shape without clearing.
- *               After MTPATTN_E_LAUNCH the main kernel may have run without the reduce
- *               that resets them: zero the header again before reusing the workspace.
+ *               Its first MTPATTN_WORKSPACE_HEADER_BYTES bytes (the counter header) must
+ *               be zero before the workspace's first use (e.g. one cudaMemset); every
+ *               call that returns MTPATTN_OK, also one that reports a device error,
+ *               leaves the tile counters zero and the two call counters equal, so the
+ *               workspace can be reused by calls of any shape without clearing.  After
+ *               MTPATTN_E_LAUNCH the main kernel may have run without the reduce that
+ *               resets the tile counters: zero the header again before reusing it.
  *               The rest need not be initialised.  Calls that overlap on the GPU must
  *               use different workspaces.
  *  out          device bf16 [total_q][num_q_heads][256]; element strides out_stride_tok,
@@ -176,7 +181,7 @@ int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_he
  * resolved segment count) return MTPATTN_E_SCRATCH_LIMIT and launch nothing.
  * The first call on each device looks up the array's device address with that
  * device current (cudaGetSymbolAddress), caches it, and clears the array's
- * 4096-byte counter header with cudaMemsetAsync on `stream`, so the clear is
+ * counter header (MTPATTN_WORKSPACE_HEADER_BYTES) with cudaMemsetAsync on `stream`, so the clear is
  * ordered before the call's kernels on any kind of stream; make that first call
  * before any stream capture.  After a call that returned MTPATTN_E_LAUNCH (its
  * reduce may not have run to reset the counters) the next call clears the

@@ -21,6 +21,7 @@ OK, E_ARG, E_UNSUPPORTED, E_DEVICE, E_WORKSPACE, E_LAUNCH = 0, -1, -2, -3, -4, -
 E_SCRATCH_LIMIT = -6
 STATIC_SCRATCH_BYTES = 32 << 20
 ERR_QLEN, ERR_QLEN_GT_SEQ, ERR_PAGE, ERR_SEQ_TOO_LONG, ERR_TIMEOUT = 1, 2, 4, 8, 16
+WORKSPACE_HEADER_BYTES = 4352     # MTPATTN_WORKSPACE_HEADER_BYTES: tile and call counters
 
 
 class MtpAttnError(RuntimeError):

@@ -7,9 +7,11 @@
 // Slots with lse = -inf (empty, or no visible key) get weight 0 and their
 // partial output is never used, so it need not have been written.  A NaN lse
 // marks a row the main kernel flagged as invalid; such rows are written as
-// zeros.  The kernel is launched as a programmatic dependent of the main kernel:
-// it may start while the main kernel drains and waits (griddepcontrol) until the
-// main kernel's results are visible.
+// zeros.  The kernel is launched as a programmatic dependent of the main kernel, so
+// its CTAs start on the SMs the main kernel's CTAs leave.  Instead of waiting for the
+// main grid to complete and flush (griddepcontrol.wait), a CTA waits until the main
+// kernel's CTAs have all counted themselves out of the workspace's call counters (each
+// after a fence behind its last write), then reads the partials from L2.
 //
 // Slot pool: when the main kernel laid the partials out unit by unit (AttnParams), a row's
 // first LSE slot holds kPoolMarker and the row's first row-slot and piece count; the row's
@@ -33,6 +35,18 @@ namespace {
 
 constexpr int kGroup = 16;          // slots per warp
 constexpr int kMaxGroups = 8;       // 2 warps each: 512 threads per CTA at most
+constexpr long long kCallWaitCycles = 4000000000LL;   // about 2 s: then MTPATTN_ERR_TIMEOUT
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {   // 2^x, hardware (rel. err ~2^-22)
   float y;
@@ -45,11 +59,26 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   // Groups 1.. hand their sums to group 0 (one row per CTA): [group - 1][half][lane].  Dynamic
   // shared memory, requested only for S > 16.
   extern __shared__ float4 xfer[];
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  __shared__ int s_timed_out;
   // The next kernel on the stream (the next call's main kernel) may start its set-up now;
   // it waits for this grid before it reads or writes anything this grid touches.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  // The main kernel is complete: put its tile counters back to zero for the next call.
+  // This grid started only after every main-kernel CTA had counted itself in, so `started`
+  // is the main grid's CTA count; wait (bounded) until all of them have counted out.
+  if (threadIdx.x == 0) {
+    const uint32_t started = ld_relaxed_gpu(p.call_ctr);
+    bool ok = ld_acquire_gpu(p.call_ctr + 1) == started;
+    if (!ok) {
+      const long long t0 = clock64();
+      while (!(ok = ld_acquire_gpu(p.call_ctr + 1) == started) && clock64() - t0 < kCallWaitCycles) {
+      }
+    }
+    s_timed_out = !ok;
+    if (!ok) set_status(p.status, MTPATTN_ERR_TIMEOUT);
+  }
+  __syncthreads();
+  // Every main-kernel CTA is done with its tiles: put the tile counters back to zero for the
+  // next call (which waits for this grid before it claims any).
   if (blockIdx.x == 0) {
     const int units = min(p.num_seqs * p.num_kv_heads, kMaxTileCounters);
     for (int i = threadIdx.x; i < units; i += blockDim.x) p.tile_ctr[i] = 0u;
@@ -69,13 +98,14 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
   // of weight 0 may hold anything, so its values are dropped by a select, never multiplied.
   const int n_spec = live ? max(0, min(min(p.slots_used, S) - s_lo, kGroup)) : 0;
   const float* lse = p.lse_part + (live ? row : 0) * S;
-  const float l0 = live && lane < S ? lse[lane] : -INFINITY;
-  const float l1 = live && lane + 32 < S ? lse[lane + 32] : -INFINITY;
+  // (loads through L2 only: no line of this call's partials may come from L1)
+  const float l0 = live && lane < S ? __ldcg(lse + lane) : -INFINITY;
+  const float l1 = live && lane + 32 < S ? __ldcg(lse + lane + 32) : -INFINITY;
   const float* ob = p.o_part + (live ? row : 0) * S * kHeadDim + part * 128 + lane * 4;
   float4 a[kGroup];
 #pragma unroll
   for (int i = 0; i < kGroup; ++i)
-    if (i < n_spec) a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s_lo + i) * kHeadDim);
+    if (i < n_spec) a[i] = __ldcg(reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s_lo + i) * kHeadDim));
   // The row's slots: P of them, LSEs lv[k] of slots lane + 32 k on each lane, partial outputs
   // from `ob`.  Slot pool (see AttnParams): the first LSE slot redirects to the row's partials
   // (honoured only if this call allowed the pool, and only inside this call's pool; otherwise
@@ -85,7 +115,7 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) lv[k] = k == 0 ? l0 : (k == 1 ? l1 : -INFINITY);
   int P = S;
-  int bad = 0;
+  int bad = s_timed_out;                           // then the partials are unknown: zeros
   bool spec = true;
   if (live && p.slot_pool && __shfl_sync(0xffffffffu, __float_as_uint(l0), 0) == kPoolMarker) {
     const int off = __shfl_sync(0xffffffffu, __float_as_int(l0), 1);
@@ -97,7 +127,7 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
     } else {
       const float* pl = p.pool_lse + off;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) lv[k] = lane + 32 * k < P ? pl[lane + 32 * k] : -INFINITY;
+      for (int k = 0; k < 8; ++k) lv[k] = lane + 32 * k < P ? __ldcg(pl + lane + 32 * k) : -INFINITY;
       ob = p.o_part + static_cast<int64_t>(off) * kHeadDim + part * 128 + lane * 4;
     }
   }
@@ -138,7 +168,7 @@ attn_reduce_kernel(const AttnParams p, int groups, int rows_per_cta) {
 #pragma unroll
       for (int i = 0; i < kGroup; ++i)
         if (i >= have && s0 + i < P && w[i] != 0.f)          // uniform across the warp
-          a[i] = *reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s0 + i) * kHeadDim);
+          a[i] = __ldcg(reinterpret_cast<const float4*>(ob + static_cast<int64_t>(s0 + i) * kHeadDim));
       // A slot of weight 0 may hold anything: its values are dropped by a select.
 #pragma unroll
       for (int i = 0; i < kGroup; ++i) {

@@ -34,6 +34,9 @@ struct AttnParams {
   int32_t num_segments;
   int32_t slots_used;    // slots most rows use (<= num_segments): the reduce loads them with the LSEs
   uint32_t* tile_ctr;    // per-unit tile counters (workspace header; zero between calls)
+  uint32_t* call_ctr;    // [2]: main-kernel CTAs started, finished (workspace header; both
+                         // only grow, equal between calls): the reduce starts merging once
+                         // every CTA of the main grid has counted itself out
   int32_t deterministic; // 1: fixed page ranges per piece (bit-identical repeats)
   int32_t scheduling;    // 0: chunks sized for max_pages, 1: pieces planned from the lengths
   float* o_part;        // [total_q * H_q][S][256] float32, normalised per segment
@@ -74,9 +77,12 @@ __device__ inline void set_status(int32_t* status, int bits) {
 
 // Host launchers (return cudaError_t of the launch).
 // Workspace header: one tile counter per (sequence, KV head) unit, up to kMaxTileCounters
-// units (beyond that the pieces keep fixed page ranges).  Zero on entry, zero on return.
+// units (beyond that the pieces keep fixed page ranges), zero on entry and on return; then
+// the two call counters (AttnParams::call_ctr), equal on entry and on return.  Zero before
+// the workspace's first use.
 constexpr int kMaxTileCounters = 1024;
-constexpr size_t kWorkspaceHeaderBytes = kMaxTileCounters * sizeof(uint32_t);
+constexpr size_t kCallCtrOffset = kMaxTileCounters * sizeof(uint32_t);
+constexpr size_t kWorkspaceHeaderBytes = kCallCtrOffset + 256;
 
 // Planned scheduling handles at most this many (sequence, KV head) units (8 per lane of the
 // planning warp), and no more units than SMs.

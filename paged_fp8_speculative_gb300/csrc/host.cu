@@ -183,6 +183,7 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
     p.pool_cap = static_cast<int32_t>(std::min<int64_t>(cap, INT32_MAX / kHeadDim));
   }
   p.tile_ctr = static_cast<uint32_t*>(workspace);
+  p.call_ctr = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kCallCtrOffset);
   p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes);
   p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeaderBytes +
                                       align_up(rows * num_segments * sizeof(float)));

@@ -46,12 +46,21 @@ def test_status_strings():
     assert api.mtp_verify_attn_strerror(-99) == "unknown status"
 
 
+def test_workspace_header_size_agrees():
+    # the header macro, the binding's constant and the library's sizing (no rows: header only)
+    src = open(os.path.join(ROOT, "include", "mtpattn.h")).read()
+    m = re.search(r"#define MTPATTN_WORKSPACE_HEADER_BYTES (\d+)", src)
+    assert m and int(m.group(1)) == api.WORKSPACE_HEADER_BYTES
+    assert api.mtp_verify_attn_workspace_size(0, 1, 1) == api.WORKSPACE_HEADER_BYTES
+
+
 def test_workspace_size():
     f = api.mtp_verify_attn_workspace_size
     rows = 64 * 16
     lse = (rows * 16 * 4 + 255) // 256 * 256
-    assert f(64, 16, 16) == 4096 + lse + rows * 16 * 256 * 4
-    assert f(7, 8, 3) == 4096 + ((7 * 8 * 3 * 4 + 255) // 256 * 256) + ((7 * 8 * 3 * 1024 + 255) // 256 * 256)
+    h = api.WORKSPACE_HEADER_BYTES
+    assert f(64, 16, 16) == h + lse + rows * 16 * 256 * 4
+    assert f(7, 8, 3) == h + ((7 * 8 * 3 * 4 + 255) // 256 * 256) + ((7 * 8 * 3 * 1024 + 255) // 256 * 256)
     assert f(64, 16, 0) == 0 and f(64, 16, 65) == 0 and f(-1, 16, 4) == 0 and f(4, 0, 4) == 0
 
 

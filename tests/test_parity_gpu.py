@@ -398,7 +398,8 @@ POOL_MARKER = 0x7fd00d1e
 def _pool_rows(ws, batch, S):
     """Output rows whose first split slot carries the slot-pool redirect."""
     rows = batch.total_q * batch.num_q_heads
-    lse = ws[4096:4096 + rows * S * 4].view(torch.int32).view(rows, S).cpu()
+    h = api.WORKSPACE_HEADER_BYTES
+    lse = ws[h:h + rows * S * 4].view(torch.int32).view(rows, S).cpu()
     return (lse[:, 0] == POOL_MARKER).nonzero().flatten().tolist()
 
 
