@@ -209,8 +209,9 @@ def _repeatable_and_graph_replay():
 
 def test_balanced_scheduling_repeats_within_reassociation(sched):
     """Balanced scheduling (the default) lets the pieces of a unit share its tiles: the
-    split differs from call to call, the result only by float32 re-association, and the
-    tile counters in the workspace header are back at zero after every call."""
+    split differs from call to call, the result only by float32 re-association, the tile
+    counters in the workspace header are back at zero after every call, and its two call
+    counters (main-kernel CTAs counted in and out) agree after every call and advance."""
     assert not api.mtp_verify_attn_get_deterministic()
     batch = synth.make_batch([5000, 5000], 4, 16, 1, seed=51, k_descale=0.5, v_descale=2.0)
     ref = oracle.verify_attention(*oracle_args(batch))
@@ -220,13 +221,19 @@ def test_balanced_scheduling_repeats_within_reassociation(sched):
     ws = torch.zeros(api.mtp_verify_attn_workspace_size(gb.total_q, 16, 16), dtype=torch.uint8,
                      device="cuda")
     outs = []
+    seen = []
     for _ in range(4):
         o = api.mtp_verify_attn_fwd(gb.q, gb.k_cache, gb.v_cache, gb.block_tables, gb.seq_lens,
                                     gb.cu_seqlens_q, kd, vd, gb.softmax_scale, num_segments=16,
                                     workspace=ws)
         torch.cuda.synchronize()
         assert ws[:4096].count_nonzero().item() == 0
+        started, finished = ws[4096:4104].view(torch.int32).tolist()
+        assert started == finished
+        seen.append(started)
         outs.append(o.float().cpu().numpy().astype(np.float64))
+    steps = np.diff(seen)
+    assert (steps > 0).all() and (steps == steps[0]).all()      # one grid's CTAs per call
     for o in outs:
         assert oracle.excess_over_half_ulp(o, ref) <= TOL
     scale = np.abs(outs[0]).max()
