@@ -17,8 +17,9 @@
 // the GPU race on it.
 //
 // The workspace's counter header (its first kWorkspaceHeaderBytes) must be zero
-// when a call starts; every call that runs both of its kernels leaves it zero
-// again, and the partials behind it need no clearing.  The header is cleared
+// before the first call; every call that runs both of its kernels leaves its tile
+// counters zero and its two call counters equal, and the partials behind it need
+// no clearing.  The header is cleared
 // with cudaMemsetAsync on the caller's stream, so the clear is ordered before
 // the call's kernels whatever kind of stream the caller uses: on the first call
 // on each device, and on the next call after one whose reduce could not be
