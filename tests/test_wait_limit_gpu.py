@@ -1,4 +1,5 @@
-"""The main kernel's bounded pipeline waits, exercised without faulting the GPU.
+"""The bounded waits of the main kernel and of the segment reduce, exercised without faulting
+the GPU.
 
 A test-only build of the library (-DMTPATTN_WAIT_CYCLES=200000, about 0.1 ms of SM clocks,
 and -DMTPATTN_TEST_STALL, which makes CTA 0's V producer skip its first tile) is called on a
@@ -76,3 +77,46 @@ def test_pipeline_wait_limit_returns_timeout_status():
     r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT, path=path)], cwd=ROOT,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_reduce_wait_limit_returns_timeout_status():
+    """The segment reduce waits, with a limit (about 2 s of SM clocks), until the main kernel's
+    CTAs have all counted themselves out of the workspace's call counters.  Two call counters
+    that disagree from the start (as in a workspace whose header was not zeroed) make that
+    wait run out: the call still returns, reports MTPATTN_ERR_TIMEOUT and writes zero rows,
+    and once the header is zeroed again the next call on the same workspace is correct."""
+    import time
+
+    import numpy as np
+    import torch
+
+    import oracle
+    from paged_fp8_speculative_gb300 import api, synth
+    from tests.helpers import oracle_args
+
+    batch = synth.make_batch([3000] * 4, 4, 16, 1, seed=32, k_descale=0.5, v_descale=2.0)
+    b = batch.to("cuda")
+    kd = torch.tensor([b.k_descale], dtype=torch.float32, device="cuda")
+    vd = torch.tensor([b.v_descale], dtype=torch.float32, device="cuda")
+    S = 8
+    ws = torch.zeros(api.mtp_verify_attn_workspace_size(b.total_q, 16, S), dtype=torch.uint8,
+                     device="cuda")
+    ws[4100:4104].view(torch.int32).fill_(12345)          # "finished" never equals "started"
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    out = api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                  b.cu_seqlens_q, kd, vd, b.softmax_scale, num_segments=S,
+                                  workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 60
+    assert status.item() & api.ERR_TIMEOUT, status.item()
+    assert out.abs().max().item() == 0
+    ws.zero_()
+    status.zero_()
+    got = api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                                  b.cu_seqlens_q, kd, vd, b.softmax_scale, num_segments=S,
+                                  workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0, status.item()
+    ref = oracle.verify_attention(*oracle_args(batch))
+    assert oracle.excess_over_half_ulp(got.float().cpu().numpy().astype(np.float64), ref) <= 0.01
