@@ -35,7 +35,14 @@
 // PV(j-1), QK(j+1), ...: QK(j+2) reuses the buffer whose P(j) PV(j) reads, and the MMAs of
 // one thread execute in issue order, so S(j + 2) complete also means PV(j) complete.  PV(j)
 // goes out in two halves: keys 0..63 once the set signals that half of P (p_half), while it
-// computes keys 64..127, and keys 64..127 at p_full.
+// computes keys 64..127, and keys 64..127 at p_full.  The widening warps arrive on the same
+// p_half barrier once the tile's f16 V is written, so one wait covers both operands.
+//
+// The MMA warp issues about 14 products per tile, and the tensor pipe takes each in 80-95
+// cycles whatever N (measured: an N = 64 QK costs what an N = 128 one does); every barrier
+// poll and tcgen05 fence in its loop leaves the pipe idle meanwhile.  So it fences only where
+// another thread's TMEM writes (P) precede the products: a K tile is written and read in the
+// async proxy (TMA, tensor cores), ordered by its barrier's transaction count alone.
 //
 // Online softmax in the log2 domain with a lazy reference m (raised, and O rescaled in TMEM,
 // only when a tile's row maximum exceeds it by more than kTau): p_s = 2^(s - m + kShift)
@@ -104,8 +111,9 @@ struct PrefillParams {
 struct PBars {
   uint64_t q_full;
   uint64_t k_full[kStagesP], k_empty[kStagesP], v_full[kStagesP], v_empty[kStagesP];
-  uint64_t v16_full[kStagesP];      // the f16 V of the stage's tile is written
-  uint64_t s_full[2], p_half[2], p_full[2], pv_done[2];   // p_half: P of keys 0..63 written
+  // p_half: P of keys 0..63 written (the set's 128 threads) and the tile's f16 V written (one
+  // arrival per widening warp)
+  uint64_t s_full[2], p_half[2], p_full[2], pv_done[2];
   uint64_t final_mma;
   uint64_t fin;                     // both sets' final m and l are published
   uint32_t tmem_base;
@@ -246,11 +254,10 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       mbar_init(smem_u32(&bars.k_empty[i]), 1);
       mbar_init(smem_u32(&bars.v_full[i]), 1);
       mbar_init(smem_u32(&bars.v_empty[i]), kConvWarps);        // one arrival per converter warp
-      mbar_init(smem_u32(&bars.v16_full[i]), kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.p_half[i]), kSetThreads);
+      mbar_init(smem_u32(&bars.p_half[i]), kSetThreads + kConvWarps);
       mbar_init(smem_u32(&bars.p_full[i]), kSetThreads);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
@@ -313,11 +320,11 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
       return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, abort_flag));
     };
     auto issue_pv = [&](int u) -> bool {
-      // P(u) in TMEM and the f16 V(u) in shared memory; the products of keys 0..63 go out as
-      // soon as their half of P is written, while the softmax works on keys 64..127
+      // P(u) in TMEM and the f16 V(u) in shared memory (both behind p_half); the products of
+      // keys 0..63 go out as soon as their half of P is written, while the softmax works on
+      // keys 64..127
       const uint32_t p_tmem = tmem + (u & 1) * 128;
       const uint32_t v_off = (u & 1) * kV16Tile;
-      if (!wait_all(bars.v16_full[u & 1], (u >> 1) & 1)) return false;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         if (!wait_all(half == 0 ? bars.p_half[u & 1] : bars.p_full[u & 1], (u >> 1) & 1))
@@ -341,7 +348,6 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
     for (int j = 0; ok && j < nt; ++j) {
       const int st = j % kStagesP;
       if (!wait_all(bars.k_full[st], (j / kStagesP) & 1)) { ok = false; break; }
-      tc_fence_after();
       if (leader) {
 #pragma unroll
         for (int k = 0; k < 6; ++k) {                 // head-dim bytes 32k .. 32k + 31 (of 192)
@@ -398,10 +404,10 @@ fmha_fp8_prefill_kernel(const __grid_constant__ PrefillParams prm) {
         *reinterpret_cast<uint4*>(dst + v16_off0 + c * 8 * 128) = w0;
         *reinterpret_cast<uint4*>(dst + v16_off1 + c * 8 * 128) = w1;
       }
-      fence_proxy_async_smem();        // visible to the tensor cores once v16_full is observed
+      fence_proxy_async_smem();        // visible to the tensor cores once p_half is observed
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&bars.v16_full[st]));
+        mbar_arrive(smem_u32(&bars.p_half[st]));      // tile j belongs to set j % 2 = st
         mbar_arrive(smem_u32(&bars.v_empty[st]));
       }
     }
