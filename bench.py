@@ -304,14 +304,16 @@ def job_tbs(kv_bytes_per_rank: int, world: int, steps: int, ms: float) -> float:
 
 # Every configuration of the workload list is also timed in the same run, the same way as
 # the headline one (cold L2 through rotating KV replicas, CUDA events around back-to-back
-# calls after warm-up): name -> (num_segments, 0 = the library's heuristic; KV replicas).
+# calls after warm-up): name -> (workload, num_segments (0 = the library's heuristic), KV
+# replicas, entry point: "exact" mtp_verify_attn_fwd, "qp_fp8" the fp8 Q/P tier).
 PER_CONFIG = {
-    "verify_16x35k_gqa16": (16, 8),
-    "verify_16x70k_gqa16": (16, 8),
-    "verify_16x35k_gqa8": (16, 8),
-    "verify_4x35k_gqa16": (64, 8),
-    "draft_extend_8": (0, 16),
-    "decode_8": (0, 16),
+    "verify_16x35k_gqa16": ("verify_16x35k_gqa16", 16, 8, "exact"),
+    "verify_16x70k_gqa16": ("verify_16x70k_gqa16", 16, 8, "exact"),
+    "verify_16x35k_gqa8": ("verify_16x35k_gqa8", 16, 8, "exact"),
+    "verify_4x35k_gqa16": ("verify_4x35k_gqa16", 64, 8, "exact"),
+    "draft_extend_8": ("draft_extend_8", 0, 16, "exact"),
+    "decode_8": ("decode_8", 0, 16, "exact"),
+    "verify_16x35k_gqa16_qp_fp8": ("verify_16x35k_gqa16", 16, 8, "qp_fp8"),
 }
 
 
@@ -352,10 +354,11 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
     process on this GPU (each with its own clock record)."""
     import torch
     res = {}
-    for name, (S0, R) in PER_CONFIG.items():
+    for name, (wl, S0, R, tier) in PER_CONFIG.items():
         if names is not None and name not in names:
             continue
-        b = synth.workload(name, seed=1, replicas=R, device="cuda")
+        fwd = api.mtp_verify_attn_fwd_qp_fp8 if tier == "qp_fp8" else api.mtp_verify_attn_fwd
+        b = synth.workload(wl, seed=1, replicas=R, device="cuda")
         tables = [b.block_tables] + b.replica_tables
         # S0 = 0: the library chooses S at every call (and may share the slots out by length)
         S = S0 or api.mtp_verify_attn_num_segments(b.num_seqs, b.num_kv_heads,
@@ -367,9 +370,8 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
         out = torch.empty_like(b.q)
 
         def call(i):
-            api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, tables[i % len(tables)],
-                                    b.seq_lens, b.cu_seqlens_q, kd, vd, b.softmax_scale,
-                                    num_segments=S0, out=out, workspace=ws, stream=stream)
+            fwd(b.q, b.k_cache, b.v_cache, tables[i % len(tables)], b.seq_lens, b.cu_seqlens_q,
+                kd, vd, b.softmax_scale, num_segments=S0, out=out, workspace=ws, stream=stream)
 
         # a short probe sizes the timed region to about a quarter of a second
         probe = time_calls(call, len(tables), max(3, warmup), 20, 0.0, stream) / 20
@@ -383,7 +385,8 @@ def per_config_numbers(api, synth, dev, stream, peak, warmup, uuid, names=None) 
                      "frac_of_8tbs_nominal": kv / (us * 1e-6) / 8e12,
                      "roofline_frac": alg_bytes_of(b) / (us * 1e-6) / 1e9 / peak,
                      "num_segments": S, "kv_replicas": R, "kv_bytes": kv, "steps": steps,
-                     "clocks": clk}
+                     "entry": "mtp_verify_attn_fwd_qp_fp8" if tier == "qp_fp8" else
+                              "mtp_verify_attn_fwd", "clocks": clk}
         del b, tables, ws, out
         torch.cuda.empty_cache()
     return res

@@ -159,6 +159,33 @@ int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_he
                         int32_t* status, void* stream);
 
 /*
+ * The same operation in the pages' precision class (aiter PR #5190 page, "Kernel notes":
+ * "Q and P are quantized to fp8"; its "Microbenchmark" notes give 0.13 sigma as that
+ * quantisation's error floor).  Arguments, workspace rules, return codes and status bits
+ * are those of mtp_verify_attn_fwd; what differs:
+ *  - each query row is scaled by a power of two (its largest |q| to [128, 256)) and rounded
+ *    once to e4m3, and each probability p * 2^(8 - 3) (at most 256) is rounded once to e4m3
+ *    before PV, instead of being carried as two e4m3 terms; the result differs from the
+ *    exact attention by up to about 0.15 of the output's standard deviation on data whose
+ *    logits are O(1), against about 0.01 for mtp_verify_attn_fwd;
+ *  - it always uses planned scheduling, whatever mtp_verify_attn_set_scheduling chose, and
+ *    returns MTPATTN_E_UNSUPPORTED (launching nothing) for batches planned scheduling does
+ *    not take: more (sequence, KV head) units than 256 or than the GPU's SMs.
+ * The two tiers run at the same speed here (the K/V stream bounds both); this one exists
+ * for callers that want the pages' numerics.
+ */
+int mtp_verify_attn_fwd_qp_fp8(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                               const void* k_cache, const void* v_cache, int64_t num_pages,
+                               const int32_t* block_tables, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                               int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                               int32_t num_kv_heads, const float* k_descale,
+                               const float* v_descale, float softmax_scale,
+                               int32_t num_segments, void* workspace, size_t workspace_bytes,
+                               void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                               int32_t* status, void* stream);
+
+/*
  * Size of the library-owned device scratch array used by
  * mtp_verify_attn_fwd_static_scratch: 32 MiB, held on every GPU that loads the
  * library until the process exits.

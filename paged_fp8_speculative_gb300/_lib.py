@@ -30,6 +30,10 @@ SIGNATURES = {
         _vp, _c_size,                   # workspace, workspace_bytes
         _vp, _c_i64, _c_i64,            # out, strides
         _vp, _vp]),                     # status, stream
+    "mtp_verify_attn_fwd_qp_fp8": (_c_int, [
+        _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _vp, _c_i32, _vp, _vp,
+        _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _c_float, _c_i32,
+        _vp, _c_size, _vp, _c_i64, _c_i64, _vp, _vp]),
     "mtp_verify_attn_fwd_static_scratch": (_c_int, [
         _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _vp, _c_i32, _vp, _vp,
         _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _c_float, _c_i32,

@@ -91,6 +91,38 @@ def _check_args(q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, kd, v
     return num_seqs, total_q, hq, k_cache.shape[2]
 
 
+def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, k_descale,
+                v_descale, softmax_scale, num_segments, out, workspace, status, stream):
+    dev = q.device
+    kd = _descale(k_descale, dev)
+    vd = _descale(v_descale, dev)
+    num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
+                                             cu_seqlens_q, kd, vd, out)
+    # None / 0: the library chooses S (and may then share the partial slots out by length);
+    # the workspace is sized for the S it will choose.
+    chosen = int(num_segments or 0)
+    S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
+                                               dev.index if dev.index is not None else -1)
+    if out is None:
+        out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    need = mtp_verify_attn_workspace_size(total_q, hq, S)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = entry(
+        _ptr(q), q.stride(0), q.stride(1),
+        _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), _ptr(cu_seqlens_q),
+        num_seqs, total_q, hq, hkv,
+        _ptr(kd), _ptr(vd), float(softmax_scale), chosen,
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), out.stride(0), out.stride(1),
+        _ptr(status), _stream_handle(stream))
+    if rc != OK:
+        raise MtpAttnError(rc)
+    return out
+
+
 def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor,
                         cu_seqlens_q: torch.Tensor, k_descale, v_descale,
@@ -110,34 +142,25 @@ def mtp_verify_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
     one is allocated for this call; a decode loop passes its own (zeroed once, reused by every
     call on the stream) so that no call allocates.
     """
-    dev = q.device
-    kd = _descale(k_descale, dev)
-    vd = _descale(v_descale, dev)
-    num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
-                                             cu_seqlens_q, kd, vd, out)
-    # None / 0: the library chooses S (and may then share the partial slots out by length);
-    # the workspace is sized for the S it will choose.
-    chosen = int(num_segments or 0)
-    S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
-                                               dev.index if dev.index is not None else -1)
-    if out is None:
-        out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    need = mtp_verify_attn_workspace_size(total_q, hq, S)
-    if workspace is None:
-        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
-    rc = lib().mtp_verify_attn_fwd(
-        _ptr(q), q.stride(0), q.stride(1),
-        _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
-        _ptr(block_tables), block_tables.shape[1],
-        _ptr(seq_lens), _ptr(cu_seqlens_q),
-        num_seqs, total_q, hq, hkv,
-        _ptr(kd), _ptr(vd), float(softmax_scale), chosen,
-        _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _ptr(out), out.stride(0), out.stride(1),
-        _ptr(status), _stream_handle(stream))
-    if rc != OK:
-        raise MtpAttnError(rc)
-    return out
+    return _verify_fwd(lib().mtp_verify_attn_fwd, q, k_cache, v_cache, block_tables, seq_lens,
+                       cu_seqlens_q, k_descale, v_descale, softmax_scale, num_segments, out,
+                       workspace, status, stream)
+
+
+def mtp_verify_attn_fwd_qp_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                               cu_seqlens_q: torch.Tensor, k_descale, v_descale,
+                               softmax_scale: float, num_segments: Optional[int] = None,
+                               out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               status: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """mtp_verify_attn_fwd with Q and P rounded once to e4m3 (the pages' precision class,
+    about 0.15 std of error instead of 0.01); planned scheduling only, so batches of more
+    (sequence, KV head) units than SMs raise MtpAttnError(E_UNSUPPORTED)."""
+    return _verify_fwd(lib().mtp_verify_attn_fwd_qp_fp8, q, k_cache, v_cache, block_tables,
+                       seq_lens, cu_seqlens_q, k_descale, v_descale, softmax_scale,
+                       num_segments, out, workspace, status, stream)
 
 
 def mtp_verify_attn_fwd_static_scratch(q: torch.Tensor, k_cache: torch.Tensor,

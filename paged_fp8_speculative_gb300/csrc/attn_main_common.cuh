@@ -26,6 +26,11 @@
 // shape one thread holds both lanes of its row, so S = hi + lo/16 is formed in registers,
 // and O = O_hi + O_lo/16 likewise in the epilogue.
 //
+// The fp8 Q/P tier (a second compilation of the planned kernel with MTPATTN_QP_FP8 set,
+// the precision class of the pages' kernel, "Q and P are quantized to fp8") keeps the same
+// layout and MMAs but writes only the hi codes: x = hi (lo rows zero) for Q, and p_s = hi
+// for P, so each is one e4m3 rounding (3 mantissa bits) of the same scaled value.
+//
 // Online softmax with a lazy reference: m is only raised (and O rescaled in TMEM) when a
 // tile's row maximum exceeds it by more than kTau (log2 units); otherwise p <= 2^kTau,
 // which the P encoding scale 2^(8 - kTau) absorbs.
@@ -127,6 +132,23 @@ __device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, u
       : "=r"(hi), "=r"(lo)
       : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
 }
+
+#if MTPATTN_QP_FP8
+// The fp8 Q/P tier (attn_main_planned_qp8.cu): x0..x3 rounded to single e4m3 codes (lowest
+// byte first, the byte order of split4's hi word), round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n"
+      " .reg .b16 a, b;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 a, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 b, %4, %3;\n"
+      " mov.b32 %0, {a, b};\n"
+      "}\n"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+#endif
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
   return __int_as_float((e + 127) << 23);

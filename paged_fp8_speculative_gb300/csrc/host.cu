@@ -95,16 +95,18 @@ extern "C" size_t mtp_verify_attn_workspace_size(int32_t total_q, int32_t num_q_
   return kWorkspaceHeaderBytes + lse + o;
 }
 
-extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
-                                   const void* k_cache, const void* v_cache, int64_t num_pages,
-                                   const int32_t* block_tables, int32_t max_pages_per_seq,
-                                   const int32_t* seq_lens, const int32_t* cu_seqlens_q,
-                                   int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
-                                   int32_t num_kv_heads, const float* k_descale,
-                                   const float* v_descale, float softmax_scale,
-                                   int32_t num_segments, void* workspace,
-                                   size_t workspace_bytes, void* out, int64_t out_stride_tok,
-                                   int64_t out_stride_head, int32_t* status, void* stream) {
+namespace {
+
+// The two precision tiers share every check and the launch set-up; qp_fp8 selects the
+// kernel that rounds Q and P to single e4m3 codes (planned scheduling only).
+int verify_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head, const void* k_cache,
+               const void* v_cache, int64_t num_pages, const int32_t* block_tables,
+               int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+               int32_t num_seqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+               const float* k_descale, const float* v_descale, float softmax_scale,
+               int32_t num_segments, void* workspace, size_t workspace_bytes, void* out,
+               int64_t out_stride_tok, int64_t out_stride_head, int32_t* status, void* stream,
+               bool qp_fp8) {
   // 1. plain argument checks
   if (num_seqs < 0 || total_q < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
       num_q_heads <= 0 || num_kv_heads <= 0)
@@ -128,6 +130,12 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   if (ratio != 8 && ratio != 16) return MTPATTN_E_UNSUPPORTED;
   if (total_q > static_cast<int64_t>(num_seqs) * MTPATTN_MAX_Q_LEN) return MTPATTN_E_UNSUPPORTED;
   if (num_segments < 0 || num_segments > MTPATTN_MAX_SEGMENTS) return MTPATTN_E_UNSUPPORTED;
+  if (qp_fp8) {                  // the fp8 tier exists for planned scheduling only
+    const int sms = device_sm_count(-1);
+    if (sms <= 0) return MTPATTN_E_DEVICE;
+    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    if (units > kPlanUnits || units > sms) return MTPATTN_E_UNSUPPORTED;
+  }
   // 3. the segment count (the heuristic needs the device) and the workspace
   int device = -1;
   const bool library_chose_s = num_segments == 0;
@@ -193,12 +201,49 @@ extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t 
   p.out_stride_head = out_stride_head;
   p.status = status;
   p.deterministic = g_deterministic.load(std::memory_order_relaxed);
-  p.scheduling = g_scheduling.load(std::memory_order_relaxed);
+  p.scheduling = qp_fp8 ? MTPATTN_SCHED_PLANNED : g_scheduling.load(std::memory_order_relaxed);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_attn_main(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
+  if ((qp_fp8 ? launch_attn_main_planned_qp8(p, st) : launch_attn_main(p, st)) != cudaSuccess)
+    return MTPATTN_E_LAUNCH;
   if (launch_attn_reduce(p, st) != cudaSuccess) return MTPATTN_E_LAUNCH;
   return MTPATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int mtp_verify_attn_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                                   const void* k_cache, const void* v_cache, int64_t num_pages,
+                                   const int32_t* block_tables, int32_t max_pages_per_seq,
+                                   const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                                   int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                   int32_t num_kv_heads, const float* k_descale,
+                                   const float* v_descale, float softmax_scale,
+                                   int32_t num_segments, void* workspace,
+                                   size_t workspace_bytes, void* out, int64_t out_stride_tok,
+                                   int64_t out_stride_head, int32_t* status, void* stream) {
+  return verify_fwd(q, q_stride_tok, q_stride_head, k_cache, v_cache, num_pages, block_tables,
+                    max_pages_per_seq, seq_lens, cu_seqlens_q, num_seqs, total_q, num_q_heads,
+                    num_kv_heads, k_descale, v_descale, softmax_scale, num_segments, workspace,
+                    workspace_bytes, out, out_stride_tok, out_stride_head, status, stream, false);
+}
+
+extern "C" int mtp_verify_attn_fwd_qp_fp8(const void* q, int64_t q_stride_tok,
+                                          int64_t q_stride_head, const void* k_cache,
+                                          const void* v_cache, int64_t num_pages,
+                                          const int32_t* block_tables, int32_t max_pages_per_seq,
+                                          const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                                          int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                          int32_t num_kv_heads, const float* k_descale,
+                                          const float* v_descale, float softmax_scale,
+                                          int32_t num_segments, void* workspace,
+                                          size_t workspace_bytes, void* out,
+                                          int64_t out_stride_tok, int64_t out_stride_head,
+                                          int32_t* status, void* stream) {
+  return verify_fwd(q, q_stride_tok, q_stride_head, k_cache, v_cache, num_pages, block_tables,
+                    max_pages_per_seq, seq_lens, cu_seqlens_q, num_seqs, total_q, num_q_heads,
+                    num_kv_heads, k_descale, v_descale, softmax_scale, num_segments, workspace,
+                    workspace_bytes, out, out_stride_tok, out_stride_head, status, stream, true);
 }
 
 extern "C" void mtp_verify_attn_set_deterministic(int32_t on) { g_deterministic.store(on ? 1 : 0); }
