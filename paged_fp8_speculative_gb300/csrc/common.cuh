@@ -92,9 +92,6 @@ constexpr int kPlanUnits = 256;
 // (attn_main_planned.cu) when p.scheduling asks for it and the batch allows it.
 cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_main_planned(AttnParams& p, cudaStream_t stream);
-// The same with Q and P rounded to single e4m3 codes (attn_main_planned_qp8.cu); planned
-// scheduling only, so the caller checks that the batch allows it.
-cudaError_t launch_attn_main_planned_qp8(AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_reduce(const AttnParams& p, cudaStream_t stream);
 // Tensor maps of the K and V caches (cached per cache, pool size and device).
 bool kv_tensor_maps(const AttnParams& p, int device, CUtensorMap* mk, CUtensorMap* mv);

@@ -12,6 +12,11 @@
 
 namespace mtpattn {
 
+// The planned main kernel with Q and P rounded to single e4m3 codes (attn_main_planned_qp8.cu,
+// where the common declaration of launch_attn_main_planned takes this name); planned
+// scheduling only, so the caller checks that the batch allows it.
+cudaError_t launch_attn_main_planned_qp8(AttnParams& p, cudaStream_t stream);
+
 int device_sm_count(int device) {
   // Filled on first use per device; atomics, since calls may come from several host threads.
   static std::atomic<int> cache[64];
