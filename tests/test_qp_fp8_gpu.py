@@ -202,3 +202,37 @@ def test_qp_fp8_refuses_batches_planned_scheduling_does_not_take():
     with pytest.raises(api.MtpAttnError) as e:
         run_tier(batch)
     assert e.value.code == api.E_UNSUPPORTED
+
+
+def test_qp_fp8_graph_replay_bit_identical():
+    """Deterministic scheduling: the tier's call captured in a CUDA graph replays bit for bit
+    like the eager call, and the descales are read on the device at replay time."""
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        batch = synth.make_batch([5000, 2000], 4, 16, 1, seed=51, kv_recipe="unit").to("cuda")
+        kd = torch.tensor([batch.k_descale], device="cuda")
+        vd = torch.tensor([batch.v_descale], device="cuda")
+        S = 8
+        ws = torch.zeros(api.mtp_verify_attn_workspace_size(batch.total_q, 16, S),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(batch.q)
+        args = (batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+                batch.cu_seqlens_q, kd, vd, batch.softmax_scale)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            api.mtp_verify_attn_fwd_qp_fp8(*args, num_segments=S, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        eager = out.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            api.mtp_verify_attn_fwd_qp_fp8(*args, num_segments=S, out=out, workspace=ws, stream=s)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+        kd.fill_(batch.k_descale * 2)
+        g.replay()
+        torch.cuda.synchronize()
+        assert not torch.equal(out, eager)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
