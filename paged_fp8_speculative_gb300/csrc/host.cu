@@ -135,12 +135,6 @@ int verify_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head, const
   if (ratio != 8 && ratio != 16) return MTPATTN_E_UNSUPPORTED;
   if (total_q > static_cast<int64_t>(num_seqs) * MTPATTN_MAX_Q_LEN) return MTPATTN_E_UNSUPPORTED;
   if (num_segments < 0 || num_segments > MTPATTN_MAX_SEGMENTS) return MTPATTN_E_UNSUPPORTED;
-  if (qp_fp8) {                  // the fp8 tier exists for planned scheduling only
-    const int sms = device_sm_count(-1);
-    if (sms <= 0) return MTPATTN_E_DEVICE;
-    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-    if (units > kPlanUnits || units > sms) return MTPATTN_E_UNSUPPORTED;
-  }
   // 3. the segment count (the heuristic needs the device) and the workspace
   int device = -1;
   const bool library_chose_s = num_segments == 0;
@@ -155,6 +149,12 @@ int verify_fwd(const void* q, int64_t q_stride_tok, int64_t q_stride_head, const
   const size_t need = mtp_verify_attn_workspace_size(total_q, num_q_heads, num_segments);
   if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < need)
     return MTPATTN_E_WORKSPACE;
+  if (qp_fp8) {                  // the fp8 tier exists for planned scheduling only
+    const int sms = device_sm_count(-1);
+    if (sms <= 0) return MTPATTN_E_DEVICE;
+    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    if (units > kPlanUnits || units > sms) return MTPATTN_E_UNSUPPORTED;
+  }
   // 4. every pointer must be memory the kernels can read on the current device
   if (device < 0 && cudaGetDevice(&device) != cudaSuccess) {
     cudaGetLastError();

@@ -78,8 +78,8 @@ def good_args(**over):
     return a
 
 
-def call(a):
-    return _lib.lib().mtp_verify_attn_fwd(
+def call(a, entry="mtp_verify_attn_fwd"):
+    return getattr(_lib.lib(), entry)(
         a["q"], a["q_st"], a["q_sh"], a["k"], a["v"], a["num_pages"], a["bt"], a["max_pages"],
         a["sl"], a["cu"], a["num_seqs"], a["total_q"], a["hq"], a["hkv"], a["kd"], a["vd"],
         a["scale"], a["S"], a["ws"], a["ws_bytes"], a["out"], a["o_st"], a["o_sh"], a["status"],
@@ -113,18 +113,25 @@ REFUSALS = [
 ]
 
 
+ENTRIES = ["mtp_verify_attn_fwd", "mtp_verify_attn_fwd_qp_fp8"]
+
+
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("over,code", REFUSALS)
-def test_refusals_before_any_launch(over, code):
-    assert call(good_args(**over)) == code
+def test_refusals_before_any_launch(over, code, entry):
+    """Both precision tiers share the checks (the fp8 tier adds its own after them)."""
+    assert call(good_args(**over), entry) == code
 
 
-def test_empty_batch_is_a_no_op():
-    assert call(good_args(num_seqs=0, total_q=0)) == api.OK
+@pytest.mark.parametrize("entry", ENTRIES)
+def test_empty_batch_is_a_no_op(entry):
+    assert call(good_args(num_seqs=0, total_q=0), entry) == api.OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_is_reported():
     assert call(good_args()) == api.E_DEVICE
+    assert call(good_args(), "mtp_verify_attn_fwd_qp_fp8") == api.E_DEVICE
     assert _lib.lib().mtp_verify_attn_num_segments(16, 1, 100, -1) == api.E_DEVICE
     assert _lib.lib().mtpattn_stream_read(FAKE, 1024, FAKE, 4, None) == api.E_DEVICE
 
