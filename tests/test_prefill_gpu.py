@@ -161,3 +161,28 @@ def test_prefill_repeatable():
     a1, _ = run(b, True)
     a2, _ = run(b, True)
     assert torch.equal(a1, a2)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_prefill_full_size_sampled(causal):
+    """The bench's shape at full size (1 x 12288 queries over 14336 keys, 96 query and KV
+    heads, one launch as the bench times it), checked on sampled row blocks of three heads.
+    A block of rows [i0, i0 + n) is the oracle's own sub-problem: those rows over the first
+    i0 + n + Lk - Lq keys (causal; bottom-right alignment then gives every row the same
+    visible keys as in the whole sequence) or over all keys (not causal)."""
+    lq, lk, hq = 12288, 14336, 96
+    b = synth.make_prefill_batch([lq], [lk], hq, hq, seed=15, device="cuda")
+    out, lse = run(b, causal)
+    got = out.float().cpu().numpy().astype(np.float64)
+    gl = lse.cpu().numpy().astype(np.float64)
+    q, k, v = b.q.cpu(), b.k.cpu(), b.v.cpu()
+    for h in (0, 47, 95):
+        for i0, n in ((0, 64), (6016, 128), (lq - 96, 96)):
+            nk = min(lk, i0 + n + lk - lq) if causal else lk
+            ref, ref_lse = oprefill.varlen_prefill_attention(
+                q[i0:i0 + n, h:h + 1].numpy(), k[:nk, h:h + 1].numpy(), v[:nk, h:h + 1].numpy(),
+                np.array([0, n]), np.array([0, nk]), b.q_descale, b.k_descale, b.v_descale,
+                causal=causal, return_lse=True)
+            res = got[i0:i0 + n, h:h + 1]
+            assert oracle.excess_over_half_ulp(res, ref) <= TOL, (h, i0)
+            assert np.abs(gl[h, i0:i0 + n] - ref_lse[0]).max() <= LSE_TOL, (h, i0)
