@@ -150,6 +150,18 @@ __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x
 }
 #endif
 
+#ifdef MTPATTN_TEST_COVERAGE
+// Test builds only: how often each (sequence, KV head, logical page) had its K streamed, one
+// counter per page of a [num_seqs][num_kv_heads][max_pages_per_seq] grid (each compilation of
+// the kernel has its own array; the including file exports a reader).
+constexpr int64_t kCoverageCounters = int64_t(1) << 22;
+static __device__ uint32_t g_coverage[kCoverageCounters];
+__device__ __forceinline__ void coverage_count(const AttnParams& p, int b, int h, int page) {
+  const int64_t i = (static_cast<int64_t>(b) * p.num_kv_heads + h) * p.max_pages + page;
+  if (i >= 0 && i < kCoverageCounters) atomicAdd(&g_coverage[i], 1u);
+}
+#endif
+
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
   return __int_as_float((e + 127) << 23);
 }

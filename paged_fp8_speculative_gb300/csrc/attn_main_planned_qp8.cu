@@ -7,4 +7,5 @@
 #define MTPATTN_QP_FP8 1
 #define attn_main_planned_kernel attn_main_planned_qp8_kernel
 #define launch_attn_main_planned launch_attn_main_planned_qp8
+#define MTPATTN_COVERAGE_READER mtpattn_test_coverage_planned_qp8
 #include "attn_main_planned.cu"

@@ -308,3 +308,18 @@ cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream) {
 }
 
 }  // namespace mtpattn
+
+#ifdef MTPATTN_TEST_COVERAGE
+// Test builds only: copy the first n page counters of this kernel to host memory, then clear
+// them (0 or a CUDA error code; -1 for a bad n).
+extern "C" int mtpattn_test_coverage_chunked(uint32_t* host_dst, int64_t n) {
+  using namespace mtpattn::mainkern;
+  if (n < 0 || n > kCoverageCounters) return -1;
+  void* dev = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&dev, g_coverage);
+  if (e == cudaSuccess) e = cudaMemcpy(host_dst, dev, n * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(dev, 0, n * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return static_cast<int>(e);
+}
+#endif
