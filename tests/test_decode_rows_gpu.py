@@ -70,7 +70,8 @@ BATCHES = {
 
 
 @pytest.mark.parametrize("det", [False, True], ids=["balanced", "fixed"])
-@pytest.mark.parametrize("sched", [api.SCHED_PLANNED, api.SCHED_CHUNKED], ids=["planned", "chunked"])
+@pytest.mark.parametrize("sched", [api.SCHED_PLANNED, api.SCHED_CHUNKED],
+                         ids=["planned", "chunked"])
 @pytest.mark.parametrize("name", list(BATCHES))
 def test_decode_rows_bit_identical_to_verify_rows(name, sched, det):
     batch = BATCHES[name]()
@@ -96,7 +97,8 @@ def header_counters(ws: torch.Tensor):
     return words[:1024].clone(), int(words[1024]), int(words[1025])
 
 
-@pytest.mark.parametrize("sched", [api.SCHED_PLANNED, api.SCHED_CHUNKED], ids=["planned", "chunked"])
+@pytest.mark.parametrize("sched", [api.SCHED_PLANNED, api.SCHED_CHUNKED],
+                         ids=["planned", "chunked"])
 def test_each_call_runs_its_kernels_once(sched):
     batch = synth.make_batch([700, 33, 2500], [4, 2, 1], 16, 1, seed=73).to("cuda")
     S = 4
