@@ -6,6 +6,7 @@ the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import contextlib
 import math
 from typing import Optional
 
@@ -56,6 +57,23 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
 
 
+def _on_call_stream(stream, device):
+    """(context, handle) for a call on `device`: the context makes the stream the call runs on
+    (`stream`, a torch stream or a raw handle, else the device's current stream) current, so
+    that the temporaries a wrapper makes inside it (descale copies, a zeroed workspace, outputs)
+    are written in that stream's order, before the library's kernels read them, and their
+    memory is not handed out again while those kernels may still use it."""
+    if device.type != "cuda":
+        return contextlib.nullcontext(), None
+    if isinstance(stream, torch.cuda.Stream):
+        ts = stream
+    elif stream is None:
+        ts = torch.cuda.current_stream(device)
+    else:
+        ts = torch.cuda.ExternalStream(int(stream), device=device)
+    return torch.cuda.stream(ts), ts.cuda_stream
+
+
 def _descale(x, device) -> torch.Tensor:
     if isinstance(x, torch.Tensor):
         return x
@@ -94,20 +112,22 @@ def _check_args(q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, kd, v
 def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, k_descale,
                 v_descale, softmax_scale, num_segments, out, workspace, status, stream):
     dev = q.device
-    kd = _descale(k_descale, dev)
-    vd = _descale(v_descale, dev)
-    num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
-                                             cu_seqlens_q, kd, vd, out)
-    # None / 0: the library chooses S (and may then share the partial slots out by length);
-    # the workspace is sized for the S it will choose.
-    chosen = int(num_segments or 0)
-    S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
-                                               dev.index if dev.index is not None else -1)
-    if out is None:
-        out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    need = mtp_verify_attn_workspace_size(total_q, hq, S)
-    if workspace is None:
-        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    ctx, handle = _on_call_stream(stream, dev)
+    with ctx:
+        kd = _descale(k_descale, dev)
+        vd = _descale(v_descale, dev)
+        num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
+                                                 cu_seqlens_q, kd, vd, out)
+        # None / 0: the library chooses S (and may then share the partial slots out by
+        # length); the workspace is sized for the S it will choose.
+        chosen = int(num_segments or 0)
+        S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
+                                                   dev.index if dev.index is not None else -1)
+        if out is None:
+            out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        need = mtp_verify_attn_workspace_size(total_q, hq, S)
+        if workspace is None:
+            workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     rc = entry(
         _ptr(q), q.stride(0), q.stride(1),
         _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
@@ -117,7 +137,7 @@ def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q
         _ptr(kd), _ptr(vd), float(softmax_scale), chosen,
         _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), out.stride(0), out.stride(1),
-        _ptr(status), _stream_handle(stream))
+        _ptr(status), handle if handle is not None else _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return out
@@ -228,10 +248,13 @@ def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, 
         blocks = int(lib().mtpattn_stream_read_default_blocks())
         if blocks <= 0:
             raise MtpAttnError(blocks)
-    if sink is None:
-        sink = torch.empty(blocks, dtype=torch.int32, device=buf.device)
+    ctx, handle = _on_call_stream(stream, buf.device)
+    with ctx:
+        if sink is None:
+            sink = torch.empty(blocks, dtype=torch.int32, device=buf.device)
     nbytes = buf.numel() * buf.element_size()
-    rc = lib().mtpattn_stream_read(_ptr(buf), nbytes, _ptr(sink), blocks, _stream_handle(stream))
+    rc = lib().mtpattn_stream_read(_ptr(buf), nbytes, _ptr(sink), blocks,
+                                   handle if handle is not None else _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return sink
@@ -271,29 +294,33 @@ def fmha_fwd_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_des
     if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must both have num_seqs + 1 entries")
     dev = q.device
-    qd, kd, vd = (_descale(x, dev) for x in (q_descale, k_descale, v_descale))
-    for name, t in (("q_descale", qd), ("k_descale", kd), ("v_descale", vd)):
-        if t.dtype != torch.float32 or t.numel() != 1:
-            raise ValueError(f"{name} must be a 1-element float32 tensor")
-    total_q, hq, _ = q.shape
-    total_k, hkv, _ = k.shape
-    if out is None:
-        out = torch.empty(total_q, hq, HEAD_DIM_V, dtype=torch.bfloat16, device=dev)
-    if out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM_V) or \
-            out.stride(2) != 1:
-        raise ValueError("out must be bf16 [total_q, H_q, 128] with unit stride on the head dim")
-    if return_lse and lse is None:
-        lse = torch.empty(hq, total_q, dtype=torch.float32, device=dev)
-    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (hq, total_q) or
-                            not lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous float32 [H_q, total_q] tensor")
+    ctx, handle = _on_call_stream(stream, dev)
+    with ctx:
+        qd, kd, vd = (_descale(x, dev) for x in (q_descale, k_descale, v_descale))
+        for name, t in (("q_descale", qd), ("k_descale", kd), ("v_descale", vd)):
+            if t.dtype != torch.float32 or t.numel() != 1:
+                raise ValueError(f"{name} must be a 1-element float32 tensor")
+        total_q, hq, _ = q.shape
+        total_k, hkv, _ = k.shape
+        if out is None:
+            out = torch.empty(total_q, hq, HEAD_DIM_V, dtype=torch.bfloat16, device=dev)
+        if out.dtype != torch.bfloat16 or tuple(out.shape) != (total_q, hq, HEAD_DIM_V) or \
+                out.stride(2) != 1:
+            raise ValueError("out must be bf16 [total_q, H_q, 128] with unit stride on the head "
+                             "dim")
+        if return_lse and lse is None:
+            lse = torch.empty(hq, total_q, dtype=torch.float32, device=dev)
+        if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (hq, total_q)
+                                or not lse.is_contiguous()):
+            raise ValueError("lse must be a contiguous float32 [H_q, total_q] tensor")
     scale = 1.0 / math.sqrt(HEAD_DIM_QK) if softmax_scale is None else float(softmax_scale)
     rc = lib().fmha_fwd_fp8_varlen(
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         cu_seqlens_q.numel() - 1, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
         _ptr(qd), _ptr(kd), _ptr(vd), scale, 1 if is_causal else 0,
-        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(status), _stream_handle(stream))
+        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(status),
+        handle if handle is not None else _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return (out, lse) if return_lse else out
