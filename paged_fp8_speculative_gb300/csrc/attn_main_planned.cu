@@ -24,6 +24,7 @@
 #include "attn_main_common.cuh"
 
 #include <algorithm>
+#include <atomic>
 
 namespace mtpattn {
 namespace {
@@ -593,12 +594,12 @@ cudaError_t launch_attn_main_planned(AttnParams& p, cudaStream_t stream) {
   prm.inv_seqs = 1.f / static_cast<float>(p.num_seqs);
   prm.inv_per = 1.f / static_cast<float>(per);
   prm.a = p;
-  static bool attr_set[64] = {false};
-  if (!attr_set[dev]) {
+  static std::atomic<bool> attr_set[64];   // per device; setting it twice is harmless
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(attn_main_planned_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(prm.num_chunks));

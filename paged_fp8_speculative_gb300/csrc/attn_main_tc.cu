@@ -19,6 +19,7 @@
 #include "attn_main_common.cuh"
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace mtpattn {
@@ -284,12 +285,12 @@ cudaError_t launch_attn_main(AttnParams& p, cudaStream_t stream) {
     p.slots_used = static_cast<int32_t>(std::min<int64_t>(touch, p.num_segments));
   }
   prm.a = p;
-  static bool attr_set[64] = {false};
-  if (!attr_set[dev]) {
+  static std::atomic<bool> attr_set[64];   // per device; setting it twice is harmless
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(attn_main_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int grid = static_cast<int>(prm.num_chunks < sms0 ? prm.num_chunks : sms0);
   cudaLaunchConfig_t cfg = {};

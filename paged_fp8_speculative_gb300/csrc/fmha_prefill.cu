@@ -56,6 +56,7 @@
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace mtpattn {
@@ -769,15 +770,15 @@ extern "C" int fmha_fwd_fp8_varlen(const void* q, int64_t q_stride_tok, int64_t 
   prm.status = status;
   const int64_t grid = static_cast<int64_t>(prm.n_qtiles) * num_q_heads * num_seqs;
   if (grid > 0x7fffffff) return MTPATTN_E_UNSUPPORTED;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];   // per device; setting it twice is harmless
   if (device >= 64) return MTPATTN_E_DEVICE;
-  if (!attr_set[device]) {
+  if (!attr_set[device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(fmha_fp8_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemP) != cudaSuccess) {
       cudaGetLastError();
       return MTPATTN_E_LAUNCH;
     }
-    attr_set[device] = true;
+    attr_set[device].store(true, std::memory_order_release);
   }
   fmha_fp8_prefill_kernel<<<static_cast<unsigned>(grid), kThreadsP, kSmemP,
                             static_cast<cudaStream_t>(stream)>>>(prm);
