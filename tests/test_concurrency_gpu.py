@@ -116,3 +116,53 @@ def test_wrapper_temporaries_follow_the_call_stream():
         torch.cuda.synchronize()
     finally:
         api.mtp_verify_attn_set_deterministic(False)
+
+
+def test_calls_from_several_host_threads():
+    """Host threads calling at once (the ctypes calls release the interpreter lock): the
+    library's per-device caches (tensor maps, kernel attributes) are shared by them.  Each
+    thread has its own stream, workspace and output; every output must equal the same call
+    made alone, bit for bit (deterministic mode)."""
+    import threading
+    batches = [synth.make_batch([2000 + 700 * i, 300, 5000 - 900 * i], [4, 2, 3], 16, 1,
+                                seed=96 + i).to("cuda") for i in range(4)]
+    S = 6
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        refs = []
+        for b in batches:
+            refs.append(api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables,
+                                                b.seq_lens, b.cu_seqlens_q, b.k_descale,
+                                                b.v_descale, b.softmax_scale, num_segments=S))
+        torch.cuda.synchronize()
+        errors = []
+
+        def worker(i):
+            try:
+                b = batches[i]
+                s = torch.cuda.Stream()
+                ws = torch.zeros(api.mtp_verify_attn_workspace_size(b.total_q, b.num_q_heads, S),
+                                 dtype=torch.uint8, device="cuda")
+                out = torch.empty_like(b.q)
+                torch.cuda.synchronize()
+                for _ in range(20):
+                    api.mtp_verify_attn_fwd(b.q, b.k_cache, b.v_cache, b.block_tables,
+                                            b.seq_lens, b.cu_seqlens_q, b.k_descale,
+                                            b.v_descale, b.softmax_scale, num_segments=S,
+                                            out=out, workspace=ws, stream=s)
+                s.synchronize()
+                if not torch.equal(out.view(torch.int16), refs[i].view(torch.int16)):
+                    errors.append(f"thread {i}: output differs")
+            except Exception as e:                      # reported below, in the test's thread
+                errors.append(f"thread {i}: {e!r}")
+
+        threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(batches))]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join(timeout=300)
+        assert not any(t.is_alive() for t in threads)
+        torch.cuda.synchronize()
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+    assert not errors, errors
