@@ -57,7 +57,9 @@ extern "C" {
  *  out           device bf16 [total_q][num_q_heads][128]; element strides out_stride_tok,
  *                out_stride_head (multiples of 8), unit stride along the head dim.
  *  lse           optional device float32 [num_q_heads][total_q] (NULL = not written).
- *  status        optional device int32; FMHA_FP8_ERR_CU is OR-ed into it.
+ *  status        optional device int32; FMHA_FP8_ERR_CU is OR-ed into it, and
+ *                MTPATTN_ERR_TIMEOUT if a CTA's pipeline wait ran out (about two seconds
+ *                without progress): that CTA's rows and LSEs are then left unwritten.
  *  stream        cudaStream_t as void*.
  * Returns MTPATTN_OK, or MTPATTN_E_ARG / _E_UNSUPPORTED / _E_DEVICE / _E_LAUNCH (see
  * mtpattn.h) before any launch.  One kernel is launched.

@@ -69,14 +69,70 @@ _CHILD = textwrap.dedent("""
 """)
 
 
-def test_pipeline_wait_limit_returns_timeout_status():
+@pytest.fixture(scope="module")
+def stall_lib():
+    """The test-only build (short wait limit, CTA 0 skipping its first V tile), built once."""
     from paged_fp8_speculative_gb300 import build
     path = os.path.join(build.BUILD, "libmtpattn_stall.so")
     build.build(extra_flags=("-DMTPATTN_WAIT_CYCLES=200000", "-DMTPATTN_TEST_STALL=1"),
                 lib_path=path)
-    r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT, path=path)], cwd=ROOT,
-                       capture_output=True, text=True, timeout=600)
+    return path
+
+
+def test_pipeline_wait_limit_returns_timeout_status(stall_lib):
+    r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT, path=stall_lib)],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+_PREFILL_CHILD = textwrap.dedent("""
+    import ctypes, sys
+    import torch
+    sys.path.insert(0, {root!r})
+    from paged_fp8_speculative_gb300 import _lib, api, synth
+
+    stall = _lib.load({path!r})
+    lq, lk = [300, 200], [700, 260]
+    b = synth.make_prefill_batch(lq, lk, 4, 2, seed=33).to("cuda")
+    H = 4
+    desc = [torch.tensor([x], dtype=torch.float32, device="cuda")
+            for x in (b.q_descale, b.k_descale, b.v_descale)]
+    ref = api.fmha_fwd_fp8_varlen(b.q, b.k, b.v, *desc, b.cu_seqlens_q, b.cu_seqlens_k,
+                                  max(lq), max(lk))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out = torch.full_like(ref, 7.0)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        rc = stall.fmha_fwd_fp8_varlen(
+            b.q.data_ptr(), b.q.stride(0), b.q.stride(1), b.k.data_ptr(), b.k.stride(0),
+            b.k.stride(1), b.v.data_ptr(), b.v.stride(0), b.v.stride(1),
+            b.cu_seqlens_q.data_ptr(), b.cu_seqlens_k.data_ptr(), len(lq), sum(lq), sum(lk),
+            max(lq), max(lk), H, 2, desc[0].data_ptr(), desc[1].data_ptr(), desc[2].data_ptr(),
+            ctypes.c_float(1.0 / 192 ** 0.5), 0, out.data_ptr(), out.stride(0), out.stride(1),
+            None, status.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, rc
+        torch.cuda.synchronize()                      # the call returned
+        assert status.item() & api.ERR_TIMEOUT, status.item()
+        # CTA 0 (the first 128 queries of sequence 0, head 0) gave up without writing;
+        # every other row is the product library's
+        assert bool((out[:128, 0] == 7.0).all())
+        keep = torch.ones(out.shape[:2], dtype=torch.bool, device="cuda")
+        keep[:128, 0] = False
+        assert torch.equal(out[keep].view(torch.int16), ref[keep].view(torch.int16))
+    print("prefill wait-limit test ok")
+""")
+
+
+def test_prefill_wait_limit_returns_timeout_status(stall_lib):
+    """The prefill's bounded waits: in the test-only build, CTA 0's TMA warp never issues its
+    first V tile, so the widening warps' wait for it runs out after about 0.1 ms; the CTA
+    raises its abort flag, every role winds down, its tensor memory is freed and its rows are
+    left unwritten, the call reports MTPATTN_ERR_TIMEOUT, and every other CTA's rows are
+    exact.  A second call returns the same way (so the first freed its resources)."""
+    r = subprocess.run([sys.executable, "-c", _PREFILL_CHILD.format(root=ROOT, path=stall_lib)],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "prefill wait-limit test ok" in r.stdout
 
 
 def test_reduce_wait_limit_returns_timeout_status():
