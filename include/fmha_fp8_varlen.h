@@ -37,7 +37,8 @@ extern "C" {
 #define FMHA_FP8_HEAD_DIM_V 128
 
 /* Device-side error bit (OR-ed into the optional status word): a sequence's cu_seqlens
- * entries fall outside [0, total] or decrease.  Its rows are not written. */
+ * entries fall outside [0, total] or decrease, or it has more queries than max_seqlen_q.
+ * Its rows are not written. */
 #define FMHA_FP8_ERR_CU 32
 
 /*
@@ -48,8 +49,9 @@ extern "C" {
  *  v             device e4m3 [total_k][num_kv_heads][128], strides as for q.
  *  cu_seqlens_q  device int32 [num_seqs + 1], 0 .. total_q, non-decreasing.
  *  cu_seqlens_k  device int32 [num_seqs + 1], 0 .. total_k, non-decreasing.
- *  max_seqlen_q  host int, >= every Lq (sizes the grid); max_seqlen_k is accepted for the
- *                page's signature and only checked to be >= 0.
+ *  max_seqlen_q  host int, >= every Lq (sizes the grid; 0 with total_q > 0 is refused with
+ *                MTPATTN_E_ARG); max_seqlen_k is accepted for the page's signature and only
+ *                checked to be >= 0.
  *  num_q_heads   a multiple of num_kv_heads.
  *  q_descale, k_descale, v_descale   device float32, one element each.
  *  softmax_scale host float (the page's default is 1/sqrt(192); pass it explicitly).

@@ -732,7 +732,8 @@ extern "C" int fmha_fwd_fp8_varlen(const void* q, int64_t q_stride_tok, int64_t 
       !aligned(k_descale, 4) || !aligned(v_descale, 4) || !aligned(lse, 4) || !aligned(status, 4))
     return MTPATTN_E_ARG;
   if (num_q_heads % num_kv_heads) return MTPATTN_E_UNSUPPORTED;
-  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return MTPATTN_OK;
+  if (num_seqs == 0 || total_q == 0) return MTPATTN_OK;
+  if (max_seqlen_q == 0) return MTPATTN_E_ARG;       // queries, but none per sequence
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) {
     cudaGetLastError();

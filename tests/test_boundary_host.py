@@ -225,7 +225,8 @@ def test_prefill_refusals(over, code):
 
 def test_prefill_empty_batch_is_a_no_op():
     assert prefill_call(B=0, tq=0) == api.OK
-    assert prefill_call(mq=0) == api.OK
+    assert prefill_call(tq=0, mq=0) == api.OK
+    assert prefill_call(mq=0) == api.E_ARG         # queries, but none allowed per sequence
 
 
 def test_prefill_wrapper_checks_shapes():

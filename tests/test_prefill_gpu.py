@@ -156,6 +156,23 @@ def test_prefill_bad_cu_seqlens_set_status():
     assert out[:64].abs().max().item() > 0
 
 
+def test_prefill_sequence_longer_than_max_seqlen_q_sets_status():
+    """max_seqlen_q sizes the grid: a sequence with more queries than it is flagged, not
+    half-written; the others are computed."""
+    b = synth.make_prefill_batch([300, 100], [300, 120], 2, 2, seed=15)
+    ref, _ = reference(b, False)
+    g = b.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.zeros(400, 2, 128, dtype=torch.bfloat16, device="cuda")
+    api.fmha_fwd_fp8_varlen(g.q, g.k, g.v, g.q_descale, g.k_descale, g.v_descale, g.cu_seqlens_q,
+                            g.cu_seqlens_k, 100, 300, out=out, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & api.ERR_CU
+    assert out[:300].abs().max().item() == 0                # the long sequence is not written
+    got = out[300:].float().cpu().numpy().astype(np.float64)
+    assert oracle.excess_over_half_ulp(got, ref[300:]) <= TOL
+
+
 def test_prefill_repeatable():
     b = synth.make_prefill_batch([300, 200], [400, 200], 4, 2, seed=14)
     a1, _ = run(b, True)
