@@ -41,8 +41,11 @@
  *    so a call may be captured in a CUDA graph.  The descales are read on the
  *    device for the same reason (aiter PR #5190 page, Kernel notes).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
- *  - The caller owns every buffer.  The library keeps only a per-device cache
- *    of the SM count.
+ *  - The caller owns every buffer.  The library keeps only host-side caches: the
+ *    SM count and each kernel's shared-memory attribute per device, and the TMA
+ *    tensor maps of the last few K/V caches (keyed by address and shape), all safe
+ *    to use from several host threads at once; plus the static device array of
+ *    mtp_verify_attn_fwd_static_scratch.
  *  - Return codes: MTPATTN_OK or a negative MTPATTN_E_*.  On an error return
  *    nothing was launched.  Nothing prints, throws or traps.
  */
