@@ -4,7 +4,9 @@ With softmax_scale = 0 every visible key has the same weight, so each output row
 of the V rows its query sees (times v_descale): a closed form, checked on the oracle too.  A
 negative k_descale (or a negative softmax_scale) flips the order of the logits, so the row
 maximum the online softmax tracks comes from the smallest raw logit; a negative v_descale flips
-the output's sign.  Both kernels must follow the definition for every sign.
+the output's sign.  Both kernels must follow the definition for every sign.  And q scaled by
+a power of two with the inverse softmax scale (the same logits) gives the verify kernel's
+output bit for bit, from 2^-60 to 2^60.
 """
 from __future__ import annotations
 
@@ -103,4 +105,23 @@ def test_prefill_signed_and_zero_scales_follow_the_definition(kd_sign, vd_sign, 
     assert oracle.excess_over_half_ulp(got, ref) <= TOL
     fin = np.isfinite(ref_lse)
     assert np.array_equal(fin, np.isfinite(lse.cpu().numpy()))
-    assert np.abs(lse.cpu().numpy()[fin] - ref_lse[fin]).max() <= 1e-3 * max(1.0, np.abs(ref_lse[fin]).max())
+    bound = 1e-3 * max(1.0, np.abs(ref_lse[fin]).max())
+    assert np.abs(lse.cpu().numpy()[fin] - ref_lse[fin]).max() <= bound
+
+
+@pytest.mark.parametrize("k", [-60, -20, 20, 60])
+def test_verify_q_scaled_by_a_power_of_two_with_the_inverse_scale_is_bit_identical(k):
+    """q times 2^k with softmax_scale times 2^-k: the same logits.  The kernel scales each Q row
+    by a power of two before its e4m3 split and folds the inverse into the logit scale, so the
+    output must be bit-identical to the unscaled call, from tiny to huge query magnitudes."""
+    batch = synth.make_batch([333, 1200], [4, 3], 16, 1, seed=104, kv_recipe="unit",
+                             k_descale=0.5, v_descale=2.0)
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        base = verify_run(batch, 3)
+        batch.q = (batch.q.double() * 2.0 ** k).to(torch.bfloat16)
+        batch.softmax_scale = batch.softmax_scale * 2.0 ** -k
+        scaled = verify_run(batch, 3)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+    assert np.array_equal(base, scaled)
