@@ -1,4 +1,5 @@
-"""Decode rows are verify rows, and every call runs its kernels exactly once.
+"""Decode rows are verify rows, every call runs its kernels exactly once, and a sequence's rows
+do not depend on its place in the batch.
 
 Row t of a verify sequence (context L, q_len n) attends to keys 0 .. L - n + t, the keys a
 q_len-1 decode of the same query token over a context of L - n + t + 1 keys, through the same
@@ -140,3 +141,37 @@ def test_each_call_runs_its_kernels_once(sched):
             assert int(tiles.abs().sum()) == 0
     finally:
         api.mtp_verify_attn_set_scheduling(api.SCHED_PLANNED)
+
+
+def permuted(batch: PagedBatch, perm) -> PagedBatch:
+    """The same sequences in the order `perm` (q rows, block tables, lengths moved together)."""
+    cu = batch.cu_seqlens_q.tolist()
+    rows = [r for b in perm for r in range(cu[b], cu[b + 1])]
+    ql = [cu[b + 1] - cu[b] for b in perm]
+    dev = batch.q.device
+    return PagedBatch(batch.q[rows].contiguous(), batch.k_cache, batch.v_cache,
+                      batch.block_tables[list(perm)].contiguous(),
+                      batch.seq_lens[list(perm)].contiguous(),
+                      torch.tensor([0] + list(np.cumsum(ql)), dtype=torch.int32, device=dev),
+                      batch.k_descale, batch.v_descale, batch.softmax_scale, batch.num_kv_heads,
+                      batch.page_size), rows
+
+
+@pytest.mark.parametrize("S", [1, 4, 0], ids=["S1", "S4", "library_S"])
+def test_sequence_order_does_not_change_any_row(S):
+    """Planned scheduling cuts every (sequence, KV head) unit by its length alone, so in
+    deterministic mode a unit's pieces, and the order the reduce merges them in, do not depend
+    on where the sequence sits in the batch: reordering the sequences reorders the output rows
+    and changes no bit."""
+    batch = synth.make_batch([17, 5000, 260, 1031, 9000, 3], [2, 4, 1, 3, 4, 1], 16, 2, seed=74,
+                             kv_recipe="unit").to("cuda")
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        base = run(batch, S)
+        for seed in range(3):
+            perm = np.random.default_rng(seed).permutation(batch.num_seqs).tolist()
+            pb, rows = permuted(batch, perm)
+            got = run(pb, S)
+            assert torch.equal(got.view(torch.int16), base[rows].view(torch.int16)), (perm, S)
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
