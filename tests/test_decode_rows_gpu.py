@@ -175,3 +175,20 @@ def test_sequence_order_does_not_change_any_row(S):
             assert torch.equal(got.view(torch.int16), base[rows].view(torch.int16)), (perm, S)
     finally:
         api.mtp_verify_attn_set_deterministic(False)
+
+
+def test_a_sequence_alone_equals_the_same_sequence_in_a_batch():
+    """With one segment every unit is computed whole by one CTA: a sequence's rows do not
+    depend on which other sequences share the call."""
+    batch = synth.make_batch([900, 4100, 33, 2500], [3, 4, 1, 2], 16, 1, seed=75).to("cuda")
+    api.mtp_verify_attn_set_deterministic(True)
+    try:
+        together = run(batch, 1)
+        cu = batch.cu_seqlens_q.tolist()
+        for b in range(batch.num_seqs):
+            alone, rows = permuted(batch, [b])
+            got = run(alone, 1)
+            want = together[cu[b]:cu[b + 1]]
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), b
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)

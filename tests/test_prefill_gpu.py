@@ -173,6 +173,25 @@ def test_prefill_sequence_longer_than_max_seqlen_q_sets_status():
     assert oracle.excess_over_half_ulp(got, ref[300:]) <= TOL
 
 
+def test_prefill_sequence_alone_equals_the_same_sequence_in_a_batch():
+    """Each CTA computes one (query tile, head, sequence) from that sequence's keys alone: a
+    sequence's rows and LSEs are the same bits whether it runs alone or packed with others."""
+    lq, lk = [130, 300, 64], [200, 300, 500]
+    b = synth.make_prefill_batch(lq, lk, 4, 2, seed=16)
+    out, lse = run(b, True)
+    q0 = k0 = 0
+    for i in range(len(lq)):
+        one = synth.PrefillBatch(b.q[q0:q0 + lq[i]], b.k[k0:k0 + lk[i]], b.v[k0:k0 + lk[i]],
+                                 torch.tensor([0, lq[i]], dtype=torch.int32),
+                                 torch.tensor([0, lk[i]], dtype=torch.int32), b.q_descale,
+                                 b.k_descale, b.v_descale, lq[i], lk[i])
+        o1, l1 = run(one, True)
+        assert torch.equal(o1.view(torch.int16), out[q0:q0 + lq[i]].view(torch.int16)), i
+        assert torch.equal(l1.view(torch.int32), lse[:, q0:q0 + lq[i]].view(torch.int32)), i
+        q0 += lq[i]
+        k0 += lk[i]
+
+
 def test_prefill_repeatable():
     b = synth.make_prefill_batch([300, 200], [400, 200], 4, 2, seed=14)
     a1, _ = run(b, True)
