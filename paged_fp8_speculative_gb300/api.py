@@ -57,21 +57,18 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
 
 
-def _on_call_stream(stream, device):
-    """(context, handle) for a call on `device`: the context makes the stream the call runs on
-    (`stream`, a torch stream or a raw handle, else the device's current stream) current, so
-    that the temporaries a wrapper makes inside it (descale copies, a zeroed workspace, outputs)
-    are written in that stream's order, before the library's kernels read them, and their
-    memory is not handed out again while those kernels may still use it."""
-    if device.type != "cuda":
-        return contextlib.nullcontext(), None
-    if isinstance(stream, torch.cuda.Stream):
-        ts = stream
-    elif stream is None:
-        ts = torch.cuda.current_stream(device)
-    else:
-        ts = torch.cuda.ExternalStream(int(stream), device=device)
-    return torch.cuda.stream(ts), ts.cuda_stream
+def _temporaries_on(stream, device, needed: bool):
+    """Context for the temporaries a wrapper makes for a call (descale tensors from Python
+    floats, a zeroed workspace, out, lse): when the call runs on a stream other than the
+    current one, they are made on that stream, so that they are written in its order, before
+    the library's kernels read them, and their memory is not handed out again while those
+    kernels may still use it.  Nothing to do when the call makes none, or runs on the current
+    stream (entering a stream context costs microseconds of host time per call)."""
+    if not needed or stream is None or device.type != "cuda":
+        return contextlib.nullcontext()
+    ts = stream if isinstance(stream, torch.cuda.Stream) else \
+        torch.cuda.ExternalStream(int(stream), device=device)
+    return torch.cuda.stream(ts)
 
 
 def _descale(x, device) -> torch.Tensor:
@@ -112,8 +109,9 @@ def _check_args(q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, kd, v
 def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, k_descale,
                 v_descale, softmax_scale, num_segments, out, workspace, status, stream):
     dev = q.device
-    ctx, handle = _on_call_stream(stream, dev)
-    with ctx:
+    makes = (out is None or workspace is None or not isinstance(k_descale, torch.Tensor) or
+             not isinstance(v_descale, torch.Tensor))
+    with _temporaries_on(stream, dev, makes):
         kd = _descale(k_descale, dev)
         vd = _descale(v_descale, dev)
         num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
@@ -137,7 +135,7 @@ def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q
         _ptr(kd), _ptr(vd), float(softmax_scale), chosen,
         _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), out.stride(0), out.stride(1),
-        _ptr(status), handle if handle is not None else _stream_handle(stream))
+        _ptr(status), _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return out
@@ -248,13 +246,11 @@ def mtpattn_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, 
         blocks = int(lib().mtpattn_stream_read_default_blocks())
         if blocks <= 0:
             raise MtpAttnError(blocks)
-    ctx, handle = _on_call_stream(stream, buf.device)
-    with ctx:
+    with _temporaries_on(stream, buf.device, sink is None):
         if sink is None:
             sink = torch.empty(blocks, dtype=torch.int32, device=buf.device)
     nbytes = buf.numel() * buf.element_size()
-    rc = lib().mtpattn_stream_read(_ptr(buf), nbytes, _ptr(sink), blocks,
-                                   handle if handle is not None else _stream_handle(stream))
+    rc = lib().mtpattn_stream_read(_ptr(buf), nbytes, _ptr(sink), blocks, _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return sink
@@ -294,8 +290,9 @@ def fmha_fwd_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_des
     if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must both have num_seqs + 1 entries")
     dev = q.device
-    ctx, handle = _on_call_stream(stream, dev)
-    with ctx:
+    makes = (out is None or (return_lse and lse is None) or
+             not all(isinstance(x, torch.Tensor) for x in (q_descale, k_descale, v_descale)))
+    with _temporaries_on(stream, dev, makes):
         qd, kd, vd = (_descale(x, dev) for x in (q_descale, k_descale, v_descale))
         for name, t in (("q_descale", qd), ("k_descale", kd), ("v_descale", vd)):
             if t.dtype != torch.float32 or t.numel() != 1:
@@ -319,8 +316,7 @@ def fmha_fwd_fp8_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_des
         _ptr(v), v.stride(0), v.stride(1), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         cu_seqlens_q.numel() - 1, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
         _ptr(qd), _ptr(kd), _ptr(vd), scale, 1 if is_causal else 0,
-        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(status),
-        handle if handle is not None else _stream_handle(stream))
+        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(status), _stream_handle(stream))
     if rc != OK:
         raise MtpAttnError(rc)
     return (out, lse) if return_lse else out
