@@ -249,3 +249,15 @@ def test_prefill_causal_pair_count_closed_form():
     for lq, lk in ((1, 1), (5, 3), (3, 5), (100, 100), (64, 300), (300, 64), (7, 0)):
         direct = sum(max(0, min(lk, i + lk - lq + 1)) for i in range(lq))
         assert _causal_pairs(lq, lk) == direct, (lq, lk)
+
+
+def test_wrappers_enter_no_stream_context_unless_they_must():
+    """Entering a stream context costs microseconds of host time per call, enough to make
+    short eager calls host-bound: the wrappers enter one only to make temporaries for a call
+    on a stream other than the current one."""
+    import contextlib
+    dev = torch.device("cuda", 0)
+    for stream, needed in ((None, True), (None, False), (12345, False)):
+        assert isinstance(api._temporaries_on(stream, dev, needed), contextlib.nullcontext)
+    assert isinstance(api._temporaries_on(12345, torch.device("cpu"), True),
+                      contextlib.nullcontext)
