@@ -11,7 +11,8 @@ that the first call of a fresh process, made on a non-default stream under
 balanced scheduling, matches the oracle (the one-time clear of the array's
 counter header is ordered on the caller's stream); and that a call which sets a
 device error bit leaves the shared header zero, so the next call still matches
-the workspace entry point bit for bit.
+the workspace entry point bit for bit; and, over random batches sized around the
+array, that a call is refused exactly when its partials would not fit.
 This file is collected last so a stop-at-first-failure run has run every other
 test before it; it passes alone in a fresh process as well.
 """
@@ -167,3 +168,43 @@ def test_static_scratch_first_call_on_a_side_stream_in_a_fresh_process():
     r = subprocess.run([sys.executable, "-c", _FRESH.format(root=root, tol=TOL)], cwd=root,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_static_scratch_random_batches_around_its_size():
+    """Random batches whose split-KV partials need a little less or a little more than the
+    static array: each call is refused with E_SCRATCH_LIMIT exactly when the workspace it
+    would need exceeds STATIC_SCRATCH_BYTES, and otherwise matches the workspace entry point
+    bit for bit (deterministic scheduling)."""
+    rng = np.random.default_rng(904)
+    api.mtp_verify_attn_set_deterministic(True)
+    refused = accepted = 0
+    try:
+        for case in range(24):
+            B = int(rng.integers(4, 33))
+            ql = [int(x) for x in rng.integers(1, 5, size=B)]
+            ctx = [int(x) for x in rng.integers(4, 3000, size=B)]
+            hq = int(rng.choice([8, 16]))
+            rows = sum(ql) * hq
+            # S around the value at which rows * S partial slots fill the array
+            S = int(np.clip(api.STATIC_SCRATCH_BYTES // (rows * 1028) + rng.integers(-2, 3), 1, 64))
+            b = synth.make_batch(ctx, ql, hq, 1, seed=905 + case).to("cuda")
+            kd = torch.full((1,), 0.5, dtype=torch.float32, device="cuda")
+            vd = torch.full((1,), 2.0, dtype=torch.float32, device="cuda")
+            out = torch.empty_like(b.q)
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            need = api.mtp_verify_attn_workspace_size(b.total_q, hq, S)
+            rc = _c_call(b, kd, vd, S, out, status)
+            if need > api.STATIC_SCRATCH_BYTES:
+                assert rc == api.E_SCRATCH_LIMIT, (case, need, rc)
+                refused += 1
+                continue
+            assert rc == api.OK, (case, need, rc)
+            torch.cuda.synchronize()
+            assert status.item() == 0, (case, status.item())
+            ref = _regular(b, kd, vd, S)
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), case
+            accepted += 1
+    finally:
+        api.mtp_verify_attn_set_deterministic(False)
+    assert refused > 0 and accepted > 0, (refused, accepted)
