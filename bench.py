@@ -329,8 +329,11 @@ def hold_stream(stream, cycles: int = 200_000) -> None:
     timing does not include the host's launch latency of the first call (the GPU would idle
     between the start event and the first kernel otherwise)."""
     import torch
+    sleep = getattr(torch.cuda, "_sleep", None)      # PyTorch's spin kernel (private API)
+    if sleep is None:
+        return
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(cycles)
+        sleep(cycles)
 
 
 def time_calls(call, R: int, warmup: int, steps: int, warm_seconds: float, stream,
