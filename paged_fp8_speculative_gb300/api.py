@@ -117,14 +117,15 @@ def _verify_fwd(entry, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q
         num_seqs, total_q, hq, hkv = _check_args(q, k_cache, v_cache, block_tables, seq_lens,
                                                  cu_seqlens_q, kd, vd, out)
         # None / 0: the library chooses S (and may then share the partial slots out by
-        # length); the workspace is sized for the S it will choose.
+        # length); a workspace made here is sized for the S it will choose, a given one is
+        # checked by the library.
         chosen = int(num_segments or 0)
-        S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
-                                                   dev.index if dev.index is not None else -1)
         if out is None:
             out = torch.empty(total_q, hq, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-        need = mtp_verify_attn_workspace_size(total_q, hq, S)
         if workspace is None:
+            S = chosen or mtp_verify_attn_num_segments(num_seqs, hkv, block_tables.shape[1],
+                                                       dev.index if dev.index is not None else -1)
+            need = mtp_verify_attn_workspace_size(total_q, hq, S)
             workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     rc = entry(
         _ptr(q), q.stride(0), q.stride(1),
